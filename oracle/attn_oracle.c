@@ -1,0 +1,205 @@
+/*
+ * FP64 reference ("oracle") for the fused attention forward.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or call
+ * this file; only the tests, the smoke check and the CPU-baseline leg of the
+ * benchmark do. It shares no code, header or constant with the CUDA library.
+ *
+ * What it computes is the plain definition of scaled dot-product attention,
+ * written out with no blocking, fusion or reordering:
+ *
+ *   s_ij = scale * sum_d q[b,i,h,d] * k[b,j,g,d]  (+ mask[b,i,j] if additive)
+ *   s_ij = -inf                                    if causal and j > i + (Sk - Sq)
+ *   m_i  = max_j s_ij                              (pass 1)
+ *   p_ij = exp(s_ij - m_i),  l_i = sum_j p_ij      (pass 2)
+ *   o[b,i,h,:] = sum_j (p_ij / l_i) * v[b,j,g,:]
+ *   lse[b,h,i] = m_i + ln(l_i)
+ *   a row with no finite s_ij gives o = 0, lse = -inf
+ *
+ * with g = floor(h / (Hq / Hkv)) (query heads grouped onto shared K/V heads).
+ *
+ * Sources:
+ *  - "ATB engineering guide" (hwcomputing.csdn.net/6a59a88310ee7a33f28e5ce9),
+ *    §5.1: the eager formula matmul(Q, K^T) * scale -> softmax -> matmul(., V);
+ *    §4.1 pattern 2 (attention fusion); §2.1 and §8.2 (MQA/GQA via kv_head_num,
+ *    causal flag, optional mask input).
+ *  - "CANN-ATB图优化-昇腾NPU怎么把PyTorch计算图改造成融合算子", Pattern 2:
+ *    Q·K^T -> Scale -> Mask -> Softmax -> ·V.
+ *  - "ops-transformer：Transformer算子融合与推理加速实战", §2.2 and §3.2
+ *    (the blockwise/online softmax reaches this same normalised result),
+ *    §2.4 (FP32 statistics on chip; this oracle uses FP64 throughout),
+ *    §4.2 (scale defaults to 1/sqrt(D); Q/K/V in (B,S,H,D)).
+ *
+ * Readings where the pages are silent: causal alignment is bottom-right
+ * (key j visible to query i iff j <= i + Sk - Sq); the additive mask is FP32
+ * (B,Sq,Sk) broadcast over heads; a non-finite or non-positive scale means
+ * 1/sqrt(D); a fully masked row gives o = 0 and lse = -inf.
+ *
+ * Inputs are the raw 16-bit patterns of bf16 (dtype 0) or IEEE fp16 (dtype 1)
+ * values; each is widened to double exactly.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_DTYPE_BF16 = 0, ORACLE_DTYPE_F16 = 1 };
+enum { ORACLE_MASK_NONE = 0, ORACLE_MASK_CAUSAL = 1, ORACLE_MASK_ADDITIVE = 2,
+       ORACLE_MASK_CAUSAL_ADDITIVE = 3 };
+
+/* bf16 is the upper half of an IEEE binary32: shift it back into place. */
+static double widen_bf16(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* IEEE binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double widen_f16(uint16_t bits) {
+    int sign = (bits >> 15) & 1;
+    int expo = (bits >> 10) & 0x1f;
+    int frac = bits & 0x3ff;
+    double mag;
+    if (expo == 0)
+        mag = ldexp((double)frac, -24);                 /* zero / subnormal */
+    else if (expo == 31)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(1024 + frac), expo - 25);  /* (1 + f/1024) 2^(e-15) */
+    return sign ? -mag : mag;
+}
+
+static double widen(uint16_t bits, int dtype) {
+    return dtype == ORACLE_DTYPE_F16 ? widen_f16(bits) : widen_bf16(bits);
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/*
+ * Attention for a list of (b, h) slices and the query rows [row_begin, row_end).
+ *
+ *   q    : (B, Sq, Hq, D)   16-bit patterns, row-major
+ *   k, v : (B, Sk, Hkv, D)  16-bit patterns, row-major
+ *   mask : (B, Sq, Sk) FP32, read only when mask_kind is additive
+ *   o    : (n_slices, row_end - row_begin, D)   output, FP64
+ *   lse  : (n_slices, row_end - row_begin)      output, FP64 (natural log)
+ *   psum : optional (may be NULL), (n_slices, rows): sum_j of the normalised
+ *          probabilities p_ij / l_i (1 for a row with a visible key, 0 otherwise)
+ *
+ * Returns 0 on success, -1 on an invalid argument.
+ */
+int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                    const float *mask, int mask_kind,
+                    int B, int Hq, int Hkv, int Sq, int Sk, int D, double scale,
+                    int n_slices, const int32_t *slice_b, const int32_t *slice_h,
+                    int row_begin, int row_end,
+                    double *o, double *lse, double *psum, int n_threads) {
+    if (!q || !k || !v || !o || !lse || !slice_b || !slice_h) return -1;
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return -1;
+    if (Hq % Hkv != 0) return -1;
+    if (mask_kind < ORACLE_MASK_NONE || mask_kind > ORACLE_MASK_CAUSAL_ADDITIVE) return -1;
+    int causal = (mask_kind == ORACLE_MASK_CAUSAL || mask_kind == ORACLE_MASK_CAUSAL_ADDITIVE);
+    int additive = (mask_kind == ORACLE_MASK_ADDITIVE || mask_kind == ORACLE_MASK_CAUSAL_ADDITIVE);
+    if (additive && !mask) return -1;
+    if (row_begin < 0 || row_end > Sq || row_begin > row_end) return -1;
+    if (!(scale > 0.0) || !isfinite(scale)) scale = 1.0 / sqrt((double)D);
+
+    const int group = Hq / Hkv;            /* query heads per K/V head */
+    const int rows = row_end - row_begin;
+    const long long causal_offset = (long long)Sk - (long long)Sq;
+
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+
+    for (int s = 0; s < n_slices; ++s) {
+        const int b = slice_b[s], h = slice_h[s];
+        if (b < 0 || b >= B || h < 0 || h >= Hq) return -1;
+        const int g = h / group;
+
+        /* Widen this slice's K and V once: (Sk, D) each. */
+        double *kd = (double *)malloc(sizeof(double) * ((size_t)Sk * D + 1));
+        double *vd = (double *)malloc(sizeof(double) * ((size_t)Sk * D + 1));
+        if (!kd || !vd) { free(kd); free(vd); return -1; }
+        for (long long j = 0; j < Sk; ++j)
+            for (int d = 0; d < D; ++d) {
+                size_t src = (((size_t)b * Sk + j) * Hkv + g) * D + d;
+                kd[j * D + d] = widen(k[src], dtype);
+                vd[j * D + d] = widen(v[src], dtype);
+            }
+
+        int failed = 0;
+#pragma omp parallel
+        {
+            double *srow = (double *)malloc(sizeof(double) * ((size_t)Sk + 1));
+            double *qd = (double *)malloc(sizeof(double) * (size_t)D);
+            if (!srow || !qd) {
+#pragma omp atomic write
+                failed = 1;
+            } else {
+#pragma omp for schedule(dynamic, 4)
+                for (int r = 0; r < rows; ++r) {
+                    const long long i = (long long)row_begin + r;
+                    double *orow = o + ((size_t)s * rows + r) * D;
+                    for (int d = 0; d < D; ++d)
+                        qd[d] = widen(q[(((size_t)b * Sq + i) * Hq + h) * D + d], dtype);
+
+                    /* Scores, then pass 1: the row maximum. */
+                    double m = -INFINITY;
+                    for (long long j = 0; j < Sk; ++j) {
+                        if (causal && j > i + causal_offset) { srow[j] = -INFINITY; continue; }
+                        double dot = 0.0;
+                        for (int d = 0; d < D; ++d) dot += qd[d] * kd[j * D + d];
+                        double sij = scale * dot;
+                        if (additive) sij += (double)mask[((size_t)b * Sq + i) * Sk + j];
+                        srow[j] = sij;
+                        if (sij > m) m = sij;
+                    }
+
+                    if (m == -INFINITY) {          /* no visible key */
+                        for (int d = 0; d < D; ++d) orow[d] = 0.0;
+                        lse[(size_t)s * rows + r] = -INFINITY;
+                        if (psum) psum[(size_t)s * rows + r] = 0.0;
+                        continue;
+                    }
+
+                    /* Pass 2: exponentials and their sum. */
+                    double l = 0.0;
+                    for (long long j = 0; j < Sk; ++j) {
+                        srow[j] = exp(srow[j] - m);
+                        l += srow[j];
+                    }
+
+                    /* Normalised probabilities times V. */
+                    double ps = 0.0;
+                    for (int d = 0; d < D; ++d) orow[d] = 0.0;
+                    for (long long j = 0; j < Sk; ++j) {
+                        double pij = srow[j] / l;
+                        ps += pij;
+                        for (int d = 0; d < D; ++d) orow[d] += pij * vd[j * D + d];
+                    }
+                    lse[(size_t)s * rows + r] = m + log(l);
+                    if (psum) psum[(size_t)s * rows + r] = ps;
+                }
+            }
+            free(srow);
+            free(qd);
+        }
+        free(kd);
+        free(vd);
+        if (failed) return -1;
+    }
+    return 0;
+}
