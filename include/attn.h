@@ -1,0 +1,136 @@
+/*
+ * attn.h — C ABI of the fused attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * One operation: O = softmax(scale * Q K^T + mask) V, computed in a single
+ * kernel launch with the softmax done online, block by block, so that the
+ * Sq x Sk score matrix never reaches device memory. The per-row running
+ * maximum and sum stay in FP32 on chip; both matrix products accumulate in
+ * FP32; the outputs are O in the input's 16-bit type and the FP32 row
+ * log-sum-exp.
+ *
+ * Passages that define the operation (the pages are cited by title):
+ *  [GUIDE]  "ATB engineering guide" (hwcomputing.csdn.net/6a59a88310ee7a33f28e5ce9):
+ *           §4.1 pattern 2 (MatMul(QK) + Softmax + MatMul(QKV) fused, O(N) memory),
+ *           §5.1 (the eager formula: scores * scale -> softmax -> times V),
+ *           §2.1 and §8.2 (MhaV3: head_num, kv_head_num for MQA/GQA, scale,
+ *           is_causal; the attention mask appended as an optional input),
+ *           §7 pitfall 2 (log-sum-exp for numerical stability).
+ *  [GRAPH]  "CANN-ATB图优化-昇腾NPU怎么把PyTorch计算图改造成融合算子",
+ *           Pattern 2: Q·K^T -> Scale -> Mask -> Softmax -> ·V becomes
+ *           FlashAttention(Q, K, V, mask, scale).
+ *  [OPS]    "ops-transformer：Transformer算子融合与推理加速实战":
+ *           §2.2 (online softmax, block by block), §2.4 (FP32 accumulation,
+ *           FP32 max/sum statistics on chip, cast only at write-out),
+ *           §3.2 (B and H independent, sequence blocks, local max and sum),
+ *           §4.2 ((B, S, H, D) inputs, D of 64 or 128, scale defaults to
+ *           1/sqrt(D), optional intermediate output), §6.2 (shape errors are
+ *           reported at the interface), §6.4 (empty inputs must work).
+ *  [MAP]    "CANN-ops-transformer和ATB-昇腾NPU上算子和加速库怎么配合",
+ *           paragraph on how ATB calls ops-transformer: an unsupported head
+ *           dimension falls back to standard attention there; here it is an
+ *           error code instead, because this library has no second path.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers marked "device" are CUDA device addresses on the current device;
+ *    "host" pointers are ordinary host memory. The caller owns every buffer.
+ *  - The library allocates no device memory, keeps no per-call state and
+ *    never synchronises implicitly: work is enqueued on `stream`
+ *    (a cudaStream_t; NULL is the legacy default stream).
+ *  - Every argument is checked on the host before anything is launched; a
+ *    rejected call launches nothing and writes nothing.
+ *  - Return values are attn_status codes (0 = success), as in [GUIDE] §8.1's
+ *    "status != 0 means failure" convention.
+ */
+#ifndef TRANSFORMER_ATTENTION_02_GB300_ATTN_H
+#define TRANSFORMER_ATTENTION_02_GB300_ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, without requiring the CUDA headers. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_MASK_NONE = 0,             /* every key visible                         */
+    ATTN_MASK_CAUSAL = 1,           /* key j visible to query i iff j <= i+Sk-Sq */
+    ATTN_MASK_ADDITIVE = 2,         /* FP32 mask (B, Sq, Sk) added to the logits */
+    ATTN_MASK_CAUSAL_ADDITIVE = 3   /* both                                      */
+} attn_mask_kind;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad mask kind,
+                                       Hq not a multiple of Hkv, misalignment    */
+    ATTN_ERR_UNSUPPORTED = 2,       /* D not 64/128, device is not sm_103        */
+    ATTN_ERR_CUDA = 3,              /* a CUDA runtime/driver call failed          */
+    ATTN_ERR_DEVICE_TIMEOUT = 4     /* a kernel gave up on a bounded wait         */
+} attn_status;
+
+/*
+ * attn_fwd — fused attention forward, bf16 in, bf16 O and FP32 LSE out.
+ *
+ *   q     device, bf16, (B, Sq, Hq, D)  contiguous, row-major, 16-byte aligned
+ *   k, v  device, bf16, (B, Sk, Hkv, D) contiguous, row-major, 16-byte aligned
+ *   o     device, bf16, (B, Sq, Hq, D)  written; 16-byte aligned; must not
+ *         overlap the inputs
+ *   lse   device, FP32, (B, Hq, Sq)     written; natural-log log-sum-exp of
+ *         each row of scaled (and masked) logits; 4-byte aligned
+ *   B, Hq, Hkv, Sq, Sk, D   sizes; Hq must be a multiple of Hkv (MHA: equal,
+ *         GQA: Hq/Hkv query heads share one K/V head, MQA: Hkv = 1); query
+ *         head h reads K/V head h / (Hq / Hkv); D must be 64 or 128
+ *   scale multiplies Q K^T; a value that is not finite or is <= 0 selects the
+ *         default 1/sqrt(D) ([OPS] §4.2; C has no default arguments)
+ *   mask_kind  one of attn_mask_kind; causal alignment is bottom-right
+ *   mask  device, FP32, (B, Sq, Sk), broadcast over heads, 4-byte aligned;
+ *         required for the additive kinds and ignored otherwise; -inf entries
+ *         hide a key
+ *   stream     CUDA stream to enqueue on
+ *
+ * Semantics: o[b,i,h,:] = sum_j softmax_j(s_ij) v[b,j,h/(Hq/Hkv),:] with
+ * s_ij = scale <q[b,i,h,:], k[b,j,g,:]> + mask[b,i,j]. A row with no visible
+ * key gets o = 0 and lse = -inf (never NaN). B, Hq or Sq of zero is a no-op
+ * that returns ATTN_OK; Sk = 0 makes every row such an empty row.
+ * Returns ATTN_OK once the work is enqueued (errors found by the kernel at run
+ * time are reported by attn_last_status).
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int Hq, int Hkv, int Sq, int Sk, int D,
+             float scale, int mask_kind, const float *mask, attn_stream_t stream);
+
+/*
+ * attn_last_status — synchronises `stream`, then returns and clears the
+ * current device's run-time status word: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT
+ * if any launch since the last call gave up on a bounded wait (the kernel then
+ * stops early, leaves its outputs incomplete and releases what it holds), or
+ * ATTN_ERR_CUDA if the synchronisation itself failed.
+ */
+int attn_last_status(attn_stream_t stream);
+
+/* attn_status_string — a static, human-readable name for a status code. */
+const char *attn_status_string(int code);
+
+/*
+ * attn_set_wait_timeout_ns — limit, in nanoseconds, on every wait inside the
+ * kernels (default 2e9 = 2 s; 0 restores the default). Applies to launches
+ * made after the call, process-wide. Returns ATTN_OK.
+ */
+int attn_set_wait_timeout_ns(unsigned long long ns);
+
+/*
+ * attn_debug_inject_stall — failure-detection test hook. While `on` is
+ * non-zero, every launch makes its MMA warp wait on a barrier that nothing
+ * ever signals, so the bounded wait runs out, the kernel records
+ * ATTN_ERR_DEVICE_TIMEOUT, drains its own copies in flight, frees its tensor
+ * memory and returns. Nothing faults. Returns ATTN_OK.
+ */
+int attn_debug_inject_stall(int on);
+
+/* attn_abi_version — version of this ABI (incremented on any change). */
+int attn_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TRANSFORMER_ATTENTION_02_GB300_ATTN_H */

@@ -1,0 +1,10 @@
+"""Fused attention forward for NVIDIA GB300 (sm_103a).
+
+The compute path is the CUDA library ``libattn.so`` (C ABI in
+``include/attn.h``); ``attn`` is its thin ctypes binding and ``inputs`` the
+seeded synthetic-input generator shared with the tests and the benchmark.
+"""
+from .attn import (  # noqa: F401
+    ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_OK,
+    MASK_ADDITIVE, MASK_CAUSAL, MASK_CAUSAL_ADDITIVE, MASK_NONE, AttnError, attention, attn_abi_version,
+    attn_debug_inject_stall, attn_fwd, attn_last_status, attn_set_wait_timeout_ns, attn_status_string)

@@ -1,0 +1,128 @@
+"""Python binding of the C ABI declared in ``include/attn.h``.
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library ``libattn.so``. There is no fallback of any kind; if the library has
+not been built, or the device is not an sm_103 GPU, the calls fail loudly.
+
+``attn_fwd`` and the other functions keep the C names and take raw device
+pointers (ints); ``attention`` is the torch convenience wrapper that derives
+the sizes from (B, S, H, D) tensors, allocates the outputs with PyTorch and
+raises ``AttnError`` on a non-zero status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+MASK_NONE, MASK_CAUSAL, MASK_ADDITIVE, MASK_CAUSAL_ADDITIVE = 0, 1, 2, 3
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT = 0, 1, 2, 3, 4
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str = "attn_fwd"):
+        self.code = code
+        super().__init__(f"{what} failed: {attn_status_string(code)} ({code})")
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def lib() -> ctypes.CDLL:
+    """Load libattn.so (once). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(path)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, P]
+    L.attn_fwd.restype = I
+    L.attn_last_status.argtypes = [P]
+    L.attn_last_status.restype = I
+    L.attn_status_string.argtypes = [I]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+    L.attn_set_wait_timeout_ns.restype = I
+    L.attn_debug_inject_stall.argtypes = [I]
+    L.attn_debug_inject_stall.restype = I
+    L.attn_abi_version.argtypes = []
+    L.attn_abi_version.restype = I
+    _lib = L
+    return L
+
+
+# ---------------------------------------------------------------- raw ABI
+
+def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, stream) -> int:
+    return lib().attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, stream)
+
+
+def attn_last_status(stream) -> int:
+    return lib().attn_last_status(stream)
+
+
+def attn_status_string(code: int) -> str:
+    return lib().attn_status_string(int(code)).decode()
+
+
+def attn_set_wait_timeout_ns(ns: int) -> int:
+    return lib().attn_set_wait_timeout_ns(int(ns))
+
+
+def attn_debug_inject_stall(on: bool) -> int:
+    return lib().attn_debug_inject_stall(1 if on else 0)
+
+
+def attn_abi_version() -> int:
+    return lib().attn_abi_version()
+
+
+# ------------------------------------------------------ torch convenience
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def attention(q, k, v, *, causal: bool = False, mask=None, scale=None, out=None, lse=None, stream=None):
+    """O, LSE = attention(Q, K, V) on (B, S, H, D) bf16 CUDA tensors.
+
+    mask: optional FP32 (B, Sq, Sk) additive mask (broadcast over heads).
+    scale: None selects 1/sqrt(D). out/lse: optional preallocated outputs.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 4 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (B, S, H, D)")
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or v.shape != k.shape:
+        raise ValueError("q, k, v shapes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    kind = (MASK_CAUSAL if causal else MASK_NONE) + (MASK_ADDITIVE if mask is not None else 0)
+    mptr = None
+    if mask is not None:
+        if not (mask.is_cuda and mask.dtype == torch.float32 and mask.is_contiguous()
+                and tuple(mask.shape) == (B, Sq, Sk)):
+            raise ValueError("mask must be a contiguous FP32 CUDA tensor of shape (B, Sq, Sk)")
+        mptr = mask.data_ptr()
+    sc = float("nan") if scale is None else float(scale)
+    rc = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                  B, Hq, Hkv, Sq, Sk, D, sc, kind, mptr, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc)
+    return out, lse

@@ -1,0 +1,239 @@
+// C ABI of the fused attention forward (declared in include/attn.h).
+//
+// The host side follows the launch layer described in "ops-transformer：
+// Transformer算子融合与推理加速实战" §3.2: check the arguments, derive the
+// tiling from the shapes, pack the pointers and sizes into one launch-parameter
+// struct and launch the kernel. Every check happens before anything is
+// enqueued, so a rejected call has no side effect; shape errors surface here,
+// at the interface (§6.2 of the same page).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_kernel.cuh"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+constexpr int kMaxDevices = 64;
+
+std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_debug_stall{0};
+
+// Run-time status word of each device: bit 0 = a bounded wait ran out.
+__device__ unsigned int g_device_status;
+
+struct DeviceInfo {
+    bool ready = false;
+    bool supported = false;
+    int num_sms = 0;
+    unsigned int* status = nullptr;     // device address of g_device_status
+    bool smem_attr_set[2][4][2] = {};   // [D is 128][mask kind][bf16]
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int fetch_encode_fn() {
+    if (g_encode) return ATTN_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return ATTN_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return ATTN_OK;
+}
+
+// Current device's cached properties (sm_103 check, SM count, status word).
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        if (d.supported) {
+            void* addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return ATTN_ERR_CUDA;
+            d.status = static_cast<unsigned int*>(addr);
+            if (fetch_encode_fn() != ATTN_OK) return ATTN_ERR_CUDA;
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return d.supported ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+}
+
+// 4-D map over a (B, S, H, D) 16-bit tensor, innermost first: (D, H, S, B).
+// One box = 64 head-dim columns (128 bytes, the swizzle span) x 128 rows of S.
+int encode_bshd(CUtensorMap* map, const void* base, int B, int S, int H, int D, bool bf16) {
+    const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S * H * D * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+__global__ void fill_empty_rows_kernel(uint16_t* o, size_t n_o, float* lse, size_t n_lse) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_o; i += stride) o[i] = 0;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_lse; i += stride) lse[i] = -INFINITY;
+}
+
+template <int D, bool CAUSAL, bool ADDITIVE, bool BF16>
+int launch_one(DeviceInfo& dev, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const attn::FwdParams& p, int grid, cudaStream_t stream) {
+    auto kernel = attn::attn_fwd_kernel<D, CAUSAL, ADDITIVE, BF16>;
+    constexpr int smem = attn::TileCfg<D>::kSmemBytes;
+    bool& attr = dev.smem_attr_set[D == 128][(CAUSAL ? 1 : 0) + (ADDITIVE ? 2 : 0)][BF16 ? 1 : 0];
+    if (!attr) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        attr = true;
+    }
+    kernel<<<grid, attn::kThreads, smem, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+template <int D, bool BF16>
+int launch_d(DeviceInfo& dev, int mask_kind, const CUtensorMap& tq, const CUtensorMap& tk,
+             const CUtensorMap& tv, const attn::FwdParams& p, int grid, cudaStream_t stream) {
+    switch (mask_kind) {
+        case ATTN_MASK_NONE: return launch_one<D, false, false, BF16>(dev, tq, tk, tv, p, grid, stream);
+        case ATTN_MASK_CAUSAL: return launch_one<D, true, false, BF16>(dev, tq, tk, tv, p, grid, stream);
+        case ATTN_MASK_ADDITIVE: return launch_one<D, false, true, BF16>(dev, tq, tk, tv, p, grid, stream);
+        default: return launch_one<D, true, true, BF16>(dev, tq, tk, tv, p, grid, stream);
+    }
+}
+
+bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
+
+int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                  int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, cudaStream_t stream,
+                  bool bf16) {
+    // ---- arguments (host only, nothing enqueued yet)
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (B < 0 || Hq < 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+    if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_ADDITIVE) return ATTN_ERR_INVALID_ARG;
+    const bool additive = mask_kind == ATTN_MASK_ADDITIVE || mask_kind == ATTN_MASK_CAUSAL_ADDITIVE;
+    if (additive && !mask) return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+        return ATTN_ERR_INVALID_ARG;
+    if (additive && !aligned(mask, 4)) return ATTN_ERR_INVALID_ARG;
+    if (Sq > (1 << 30) || Sk > (1 << 30)) return ATTN_ERR_INVALID_ARG;
+    const long long n_mblk = ((long long)Sq + attn::kRowsPerTile - 1) / attn::kRowsPerTile;
+    if ((long long)B * Hq * n_mblk > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if (B == 0 || Hq == 0 || Sq == 0) return ATTN_OK;        // nothing to compute
+    if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt((float)D);
+
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != ATTN_OK) return rc;
+
+    if (Sk == 0) {                                            // every row sees no key
+        const size_t n_o = (size_t)B * Sq * Hq * D, n_lse = (size_t)B * Hq * Sq;
+        fill_empty_rows_kernel<<<dev->num_sms, 256, 0, stream>>>(static_cast<uint16_t*>(o), n_o, lse, n_lse);
+        return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    }
+
+    CUtensorMap tq, tk, tv;
+    if (encode_bshd(&tq, q, B, Sq, Hq, D, bf16) != ATTN_OK || encode_bshd(&tk, k, B, Sk, Hkv, D, bf16) != ATTN_OK ||
+        encode_bshd(&tv, v, B, Sk, Hkv, D, bf16) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+
+    attn::FwdParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.mask = additive ? mask : nullptr;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.group = Hq / Hkv;
+    p.n_mblk = (int)n_mblk;
+    p.n_tiles = (int)((long long)B * Hq * n_mblk);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.mask_vec4 = additive && aligned(mask, 16) && (Sk % 4 == 0);
+    p.debug_stall = g_debug_stall.load();
+    p.timeout_ns = g_timeout_ns.load();
+    p.status = dev->status;
+
+    const int grid = p.n_tiles < dev->num_sms ? p.n_tiles : dev->num_sms;
+    if (D == 128)
+        return bf16 ? launch_d<128, true>(*dev, mask_kind, tq, tk, tv, p, grid, stream)
+                    : launch_d<128, false>(*dev, mask_kind, tq, tk, tv, p, grid, stream);
+    return bf16 ? launch_d<64, true>(*dev, mask_kind, tq, tk, tv, p, grid, stream)
+                : launch_d<64, false>(*dev, mask_kind, tq, tk, tv, p, grid, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+             int Sk, int D, float scale, int mask_kind, const float* mask, attn_stream_t stream) {
+    return attn_fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
+                         reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+int attn_last_status(attn_stream_t stream) {
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != ATTN_OK) return rc;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    unsigned int word = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&word, g_device_status, sizeof word) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (word != 0 && cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess) return ATTN_ERR_CUDA;
+    return (word & attn::kStatusTimeout) ? ATTN_ERR_DEVICE_TIMEOUT : ATTN_OK;
+}
+
+const char* attn_status_string(int code) {
+    switch (code) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+        case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT";
+        default: return "ATTN_UNKNOWN_STATUS";
+    }
+}
+
+int attn_set_wait_timeout_ns(unsigned long long ns) {
+    g_timeout_ns.store(ns ? ns : kDefaultTimeoutNs);
+    return ATTN_OK;
+}
+
+int attn_debug_inject_stall(int on) {
+    g_debug_stall.store(on ? 1 : 0);
+    return ATTN_OK;
+}
+
+int attn_abi_version(void) { return kAbiVersion; }
+
+}  // extern "C"
