@@ -86,6 +86,8 @@ typedef enum {
  *         required for the additive kinds and ignored otherwise; -inf entries
  *         hide a key
  *   stream     CUDA stream to enqueue on
+ *   A pointer may be null only when its tensor has no elements (for example
+ *   k and v when B or Sk is 0).
  *
  * Semantics: o[b,i,h,:] = sum_j softmax_j(s_ij) v[b,j,h/(Hq/Hkv),:] with
  * s_ij = scale <q[b,i,h,:], k[b,j,g,:]> + mask[b,i,j]. A row with no visible

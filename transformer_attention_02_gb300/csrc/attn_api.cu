@@ -135,11 +135,14 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
                   int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, cudaStream_t stream,
                   bool bf16) {
     // ---- arguments (host only, nothing enqueued yet)
-    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
     if (B < 0 || Hq < 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_ADDITIVE) return ATTN_ERR_INVALID_ARG;
     const bool additive = mask_kind == ATTN_MASK_ADDITIVE || mask_kind == ATTN_MASK_CAUSAL_ADDITIVE;
-    if (additive && !mask) return ATTN_ERR_INVALID_ARG;
+    // A pointer may be null only when its tensor has no elements.
+    const bool q_empty = (long long)B * Sq * Hq == 0, kv_empty = (long long)B * Sk == 0;
+    if ((!q && !q_empty) || (!o && !q_empty) || (!lse && !q_empty)) return ATTN_ERR_INVALID_ARG;
+    if ((!k && !kv_empty) || (!v && !kv_empty)) return ATTN_ERR_INVALID_ARG;
+    if (additive && !mask && !q_empty && !kv_empty) return ATTN_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
