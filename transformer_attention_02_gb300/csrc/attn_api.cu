@@ -110,6 +110,10 @@ int launch_one(DeviceInfo& dev, const CUtensorMap& tq, const CUtensorMap& tk, co
     constexpr int smem = attn::TileCfg<D>::kSmemBytes;
     bool& attr = dev.smem_attr_set[D == 128][(CAUSAL ? 1 : 0) + (ADDITIVE ? 2 : 0)][BF16 ? 1 : 0];
     if (!attr) {
+        // The in-kernel register split assumes exactly kLaunchRegs per thread at launch.
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (fa.numRegs != attn::kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return ATTN_ERR_CUDA;
         attr = true;

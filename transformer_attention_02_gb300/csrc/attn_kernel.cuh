@@ -16,11 +16,12 @@
 // walks the tiles; with a causal mask the longest tiles come first and the
 // query heads that share a K/V head are adjacent so their K/V stay in L2.
 //
-// Roles inside a CTA (320 threads):
+// Roles inside a CTA (384 threads):
 //   warps 0-3  softmax warpgroup 0: query rows [m0, m0+128)      (TMEM lanes 0-127)
 //   warps 4-7  softmax warpgroup 1: query rows [m0+128, m0+256)
 //   warp  8    MMA issuer (one thread) + TMEM allocation
 //   warp  9    TMA producer (one thread) + barrier initialisation
+//   warps 10-11 idle (they complete the third warpgroup for the register split)
 // Pipelining ("ops-transformer：…实战" §2.3): while one warpgroup exponentiates
 // its scores, the tensor cores work on the other warpgroup's tile, and the TMA
 // warp streams the next K/V tiles into a ring of shared-memory slots.
@@ -55,9 +56,17 @@ struct FwdParams {
     unsigned int* status;     // device status word, bit 0 = a wait timed out
 };
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;               // three warpgroups
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
+// Register split: launched at 168 per thread (384 x 168 = 64512), then the
+// softmax warpgroups grow to 200 and the MMA/TMA warpgroup shrinks to 104:
+// 128 x (200 + 200 + 104) = 64512. The host refuses to launch unless the
+// compiled kernel uses exactly kLaunchRegs, so the split always fits.
+constexpr int kLaunchRegs = 168;
+constexpr uint32_t kSoftmaxRegs = 200;
+constexpr uint32_t kControlRegs = 104;
+static_assert(128 * (2 * kSoftmaxRegs + kControlRegs) <= kThreads * kLaunchRegs, "register split");
 constexpr int kBlockM = 128;        // query rows per softmax warpgroup
 constexpr int kBlockN = 128;        // keys per K/V tile
 constexpr int kRowsPerTile = 2 * kBlockM;
@@ -81,13 +90,12 @@ struct TileCfg {
     static constexpr int bQEmpty = 2;
     static constexpr int bSFull = 3;        // [2]
     static constexpr int bPFull = 5;        // [2]
-    static constexpr int bPVDone = 7;       // [2]
-    static constexpr int bOFull = 9;        // [2]
-    static constexpr int bDrain = 11;
-    static constexpr int bStall = 12;
-    static constexpr int bKVFull = 13;      // [kSlots]
-    static constexpr int bKVEmpty = 13 + kSlots;
-    static constexpr int kNumBars = 13 + 2 * kSlots;
+    static constexpr int bOFull = 7;        // [2]
+    static constexpr int bDrain = 9;
+    static constexpr int bStall = 10;
+    static constexpr int bKVFull = 11;      // [kSlots]
+    static constexpr int bKVEmpty = 11 + kSlots;
+    static constexpr int kNumBars = 11 + 2 * kSlots;
     static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemUsed = kAbortOff + 4;
@@ -210,6 +218,17 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
 }
 
 // -------------------------------------------------------------- MMA issuer
+// Issue order per KV block j of a tile with n blocks (ping-pong between the two
+// query tiles, so that each softmax warpgroup works while the tensor cores run
+// the other tile's two products):
+//     prologue:  S0 = Q0 K0^T, S1 = Q1 K0^T
+//     block j:   O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T
+// S_t and P_t share TMEM columns. The write of S_t for block j+1 is issued by
+// this thread after the product that reads P_t of block j, and the tensor core
+// executes the MMAs of one issuing thread in issue order, so that read happens
+// first. Each commit covers every MMA issued before it, so "S_t ready" also
+// means that the previous O_t += P_t V has completed (the softmax may rescale
+// O_t and overwrite P_t after it).
 template <int D, bool CAUSAL, bool BF16>
 __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const SyncCtx& sc) {
     using C = TileCfg<D>;
@@ -218,64 +237,78 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
     constexpr uint32_t kIdescQK = ptx::idesc_f16(128, kBlockN, BF16, false, false);
     constexpr uint32_t kIdescPV = ptx::idesc_f16(128, D, BF16, false, true);
     uint32_t kv_use = 0, q_uses = 0;
-    uint32_t p_cnt[2] = {0, 0}, pv_cnt[2] = {0, 0};
+    uint32_t p_cnt[2] = {0, 0};
     bool issued = false;
     bool alive = true;
+
+    auto acquire = [&](uint32_t& slot) -> bool {      // next K or V tile of the ring
+        slot = kv_use % C::kSlots;
+        const bool ok = wait_phase(bar(C::bKVFull + slot), (kv_use / C::kSlots) & 1u, sc);
+        ++kv_use;
+        if (ok) ptx::tc_fence_after_sync();
+        return ok;
+    };
+    auto issue_qk = [&](int t, uint32_t k_slot) {
+        const uint32_t q_base = smem + C::kQOff + t * C::kTileBytes;
+        const uint32_t k_base = smem + C::kKVOff + k_slot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+            ptx::mma_ss(tmem + C::s_col(t), ptx::sdesc_kmajor_sw128(q_base + off),
+                        ptx::sdesc_kmajor_sw128(k_base + off), kIdescQK, kk > 0 ? 1u : 0u);
+        }
+        ptx::tc_commit(bar(C::bSFull + t));
+    };
+    auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) {
+        const uint32_t v_base = smem + C::kKVOff + v_slot * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            ptx::mma_ts(tmem + C::kOCol0 + t * D, tmem + C::s_col(t) + kk * 8,
+                        ptx::sdesc_mnmajor_sw128(v_base + kk * 16 * 128, C::kBoxBytes), kIdescPV,
+                        (accumulate || kk > 0) ? 1u : 0u);
+        }
+    };
+    auto wait_p = [&](int t) -> bool {
+        const bool ok = wait_phase(bar(C::bPFull + t), p_cnt[t] & 1u, sc);
+        ++p_cnt[t];
+        if (ok) ptx::tc_fence_after_sync();
+        return ok;
+    };
+
     if (p.debug_stall) alive = wait_phase(bar(C::bStall), 0, sc);   // nothing ever arrives
     for (int tile = blockIdx.x; tile < p.n_tiles && alive; tile += gridDim.x) {
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
-        if (ti.n_blocks == 0) continue;
+        const int n = ti.n_blocks;
+        if (n == 0) continue;
         if (!wait_phase(bar(C::bQFull + 0), q_uses & 1u, sc) ||
             !wait_phase(bar(C::bQFull + 1), q_uses & 1u, sc)) { alive = false; break; }
         ++q_uses;
         ptx::tc_fence_after_sync();
-        for (int j = 0; j < ti.n_blocks; ++j) {
-            // ---- S_t = Q_t K_j^T
-            const uint32_t ks = kv_use % C::kSlots;
-            if (!wait_phase(bar(C::bKVFull + ks), (kv_use / C::kSlots) & 1u, sc)) { alive = false; break; }
-            ++kv_use;
-            ptx::tc_fence_after_sync();
-            const uint32_t k_base = smem + C::kKVOff + ks * C::kTileBytes;
-            for (int t = 0; t < 2 && alive; ++t) {
-                // S_t still holds P_t of the previous block until that P.V is done.
-                if (pv_cnt[t] > 0) {
-                    if (!wait_phase(bar(C::bPVDone + t), (pv_cnt[t] - 1) & 1u, sc)) { alive = false; break; }
-                    ptx::tc_fence_after_sync();
-                }
-                const uint32_t q_base = smem + C::kQOff + t * C::kTileBytes;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-                    ptx::mma_ss(tmem + C::s_col(t), ptx::sdesc_kmajor_sw128(q_base + off),
-                                ptx::sdesc_kmajor_sw128(k_base + off), kIdescQK, kk > 0 ? 1u : 0u);
-                }
-                issued = true;
-                ptx::tc_commit(bar(C::bSFull + t));
+        uint32_t ks, vs;
+        if (!acquire(ks)) { alive = false; break; }
+        issue_qk(0, ks);
+        issue_qk(1, ks);
+        issued = true;
+        ptx::tc_commit(bar(C::bKVEmpty + ks));
+        if (n == 1) ptx::tc_commit(bar(C::bQEmpty));
+        for (int j = 0; j < n; ++j) {
+            const bool more = j + 1 < n;
+            if (!acquire(vs) || !wait_p(0)) { alive = false; break; }
+            issue_pv(0, vs, j > 0);
+            if (!more) ptx::tc_commit(bar(C::bOFull + 0));
+            if (more) {
+                if (!acquire(ks)) { alive = false; break; }
+                issue_qk(0, ks);
             }
-            if (!alive) break;
-            ptx::tc_commit(bar(C::bKVEmpty + ks));
-            if (j == ti.n_blocks - 1) ptx::tc_commit(bar(C::bQEmpty));
-            // ---- O_t += P_t V_j
-            const uint32_t vs = kv_use % C::kSlots;
-            if (!wait_phase(bar(C::bKVFull + vs), (kv_use / C::kSlots) & 1u, sc)) { alive = false; break; }
-            ++kv_use;
-            const uint32_t v_base = smem + C::kKVOff + vs * C::kTileBytes;
-            for (int t = 0; t < 2 && alive; ++t) {
-                if (!wait_phase(bar(C::bPFull + t), p_cnt[t] & 1u, sc)) { alive = false; break; }
-                ++p_cnt[t];
-                ptx::tc_fence_after_sync();
-#pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    ptx::mma_ts(tmem + C::kOCol0 + t * D, tmem + C::s_col(t) + kk * 8,
-                                ptx::sdesc_mnmajor_sw128(v_base + kk * 16 * 128, C::kBoxBytes), kIdescPV,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                ptx::tc_commit(bar(C::bPVDone + t));
-                ++pv_cnt[t];
-                if (j == ti.n_blocks - 1) ptx::tc_commit(bar(C::bOFull + t));
-            }
-            if (!alive) break;
+            if (!wait_p(1)) { alive = false; break; }
+            issue_pv(1, vs, j > 0);
             ptx::tc_commit(bar(C::bKVEmpty + vs));
+            if (!more) ptx::tc_commit(bar(C::bOFull + 1));
+            if (more) {
+                issue_qk(1, ks);
+                ptx::tc_commit(bar(C::bKVEmpty + ks));
+                if (j + 1 == n - 1) ptx::tc_commit(bar(C::bQEmpty));
+            }
         }
     }
     // Shut down: every MMA this thread issued must finish before TMEM is freed.
@@ -324,6 +357,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
         float m_used = -INFINITY;     // max used for the exponentials (log2 units)
         float l_sum = 0.f;
         bool ok = true;
+        const float sl = p.scale_log2;
         for (int j = 0; j < ti.n_blocks; ++j) {
             ok = wait_phase(bar(C::bSFull + wg), s_phase, sc);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -338,25 +372,29 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
 
             const int key0 = j * kBlockN;
             const int vis = kv_lim - key0;                    // columns >= vis are hidden
-            // x = s * scale * log2(e) (+ mask * log2(e)): logits in log2 units
+            // x: raw scores, or (additive mask) logits in log2 units
             float x[kBlockN];
 #pragma unroll
-            for (int c = 0; c < kBlockN; ++c) x[c] = __uint_as_float(sr[c]) * p.scale_log2;
-            if (ADDITIVE && mrow != nullptr) {
-                if (p.mask_vec4 && key0 + kBlockN <= p.Sk) {
-                    const float4* m4 = reinterpret_cast<const float4*>(mrow + key0);
+            for (int c = 0; c < kBlockN; ++c) x[c] = __uint_as_float(sr[c]);
+            if (ADDITIVE) {
 #pragma unroll
-                    for (int c = 0; c < kBlockN / 4; ++c) {
-                        const float4 mv = __ldg(m4 + c);
-                        x[4 * c + 0] = fmaf(mv.x, kLog2e, x[4 * c + 0]);
-                        x[4 * c + 1] = fmaf(mv.y, kLog2e, x[4 * c + 1]);
-                        x[4 * c + 2] = fmaf(mv.z, kLog2e, x[4 * c + 2]);
-                        x[4 * c + 3] = fmaf(mv.w, kLog2e, x[4 * c + 3]);
+                for (int c = 0; c < kBlockN; ++c) x[c] *= sl;
+                if (mrow != nullptr) {
+                    if (p.mask_vec4 && key0 + kBlockN <= p.Sk) {
+                        const float4* m4 = reinterpret_cast<const float4*>(mrow + key0);
+#pragma unroll
+                        for (int c = 0; c < kBlockN / 4; ++c) {
+                            const float4 mv = __ldg(m4 + c);
+                            x[4 * c + 0] = fmaf(mv.x, kLog2e, x[4 * c + 0]);
+                            x[4 * c + 1] = fmaf(mv.y, kLog2e, x[4 * c + 1]);
+                            x[4 * c + 2] = fmaf(mv.z, kLog2e, x[4 * c + 2]);
+                            x[4 * c + 3] = fmaf(mv.w, kLog2e, x[4 * c + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < kBlockN; ++c)
+                            if (key0 + c < p.Sk) x[c] = fmaf(__ldg(mrow + key0 + c), kLog2e, x[c]);
                     }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < kBlockN; ++c)
-                        if (key0 + c < p.Sk) x[c] = fmaf(__ldg(mrow + key0 + c), kLog2e, x[c]);
                 }
             }
             if (vis < kBlockN) {
@@ -364,15 +402,18 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
                 for (int c = 0; c < kBlockN; ++c)
                     if (c >= vis) x[c] = -INFINITY;
             }
-            float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
+            float mA = fmaxf(x[0], x[1]), mB = fmaxf(x[2], x[3]);
+            float mC = fmaxf(x[4], x[5]), mD = fmaxf(x[6], x[7]);
 #pragma unroll
-            for (int c = 4; c < kBlockN; c += 4) {
-                mx0 = fmaxf(mx0, x[c + 0]);
-                mx1 = fmaxf(mx1, x[c + 1]);
-                mx2 = fmaxf(mx2, x[c + 2]);
-                mx3 = fmaxf(mx3, x[c + 3]);
+            for (int c = 8; c < kBlockN; c += 8) {
+                mA = ptx::max3(mA, x[c + 0], x[c + 1]);
+                mB = ptx::max3(mB, x[c + 2], x[c + 3]);
+                mC = ptx::max3(mC, x[c + 4], x[c + 5]);
+                mD = ptx::max3(mD, x[c + 6], x[c + 7]);
             }
-            const float m_new = fmaxf(m_used, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)));
+            float m_blk = fmaxf(fmaxf(mA, mB), fmaxf(mC, mD));
+            if (!ADDITIVE) m_blk *= sl;                       // scale > 0 keeps the order
+            const float m_new = fmaxf(m_used, m_blk);
             float alpha = 1.f;
             bool rescale = false;
             if (j == 0) {
@@ -386,23 +427,30 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
                     m_used = m_new;
                 }
             }
-            const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+            const float nm = (m_used == -INFINITY) ? 0.f : -m_used;
             uint32_t pk[kBlockN / 2];
-            float ls0 = 0.f, ls1 = 0.f;
+            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
             for (int c = 0; c < kBlockN / 2; ++c) {
-                const float p0 = ptx::ex2(x[2 * c] - m_ref);
-                const float p1 = ptx::ex2(x[2 * c + 1] - m_ref);
-                ls0 += p0;
-                ls1 += p1;
-                pk[c] = BF16 ? ptx::pack_bf16x2(p0, p1) : ptx::pack_f16x2(p0, p1);
+                float a, b;
+                if (ADDITIVE)
+                    ptx::add2(a, b, x[2 * c], x[2 * c + 1], nm, nm);
+                else
+                    ptx::fma2(a, b, x[2 * c], x[2 * c + 1], sl, sl, nm, nm);
+                a = ptx::ex2(a);
+                b = ptx::ex2(b);
+                if (c & 1)
+                    ptx::add2(l2, l3, l2, l3, a, b);
+                else
+                    ptx::add2(l0, l1, l0, l1, a, b);
+                pk[c] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
             }
-            l_sum += ls0 + ls1;
+            l_sum += (l0 + l1) + (l2 + l3);
             ptx::tmem_st32(tS + 0, pk);
             ptx::tmem_st32(tS + 32, pk + 32);
             if (rescale) {
-                // O_t holds the previous blocks' sum and no P.V is running on it:
-                // this S_t was computed only after that P.V had completed.
+                // O_t holds the sum over the previous blocks and no product is
+                // running on it: "S_t ready" covered the previous O_t += P_t V.
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t ov[32];
@@ -491,13 +539,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const SyncCtx sc{abort_flag, p.status, p.timeout_ns};
 
     if (warp < 8) {
+        ptx::setmaxnreg_inc<kSoftmaxRegs>();
         role_softmax<D, CAUSAL, ADDITIVE, BF16>(p, smem, tmem, warp >> 2, sc);
-    } else if (warp == kMmaWarp) {
-        if (lane == 0) role_mma<D, CAUSAL, BF16>(p, smem, tmem, sc);
-        __syncwarp();
-    } else if (warp == kTmaWarp) {
-        if (lane == 0) role_tma<D, CAUSAL>(&tmQ, &tmK, &tmV, p, smem, sc);
-        __syncwarp();
+    } else {
+        ptx::setmaxnreg_dec<kControlRegs>();
+        if (warp == kMmaWarp) {
+            if (lane == 0) role_mma<D, CAUSAL, BF16>(p, smem, tmem, sc);
+            __syncwarp();
+        } else if (warp == kTmaWarp) {
+            if (lane == 0) role_tma<D, CAUSAL>(&tmQ, &tmK, &tmV, p, smem, sc);
+            __syncwarp();
+        }
     }
 
     ptx::tc_fence_before_sync();
