@@ -108,9 +108,14 @@ struct TileCfg {
 };
 
 struct TileInfo {
-    int b, h, hk, m0, n_blocks;
+    int b, h, hk, m0;
+    int nb[2];      // KV blocks needed by query sub-tile t (rows m0+128t .. m0+128t+127)
+    int n;          // max(nb[0], nb[1]): KV blocks streamed for the tile
 };
 
+// Work tiles in order: with a causal mask the longest first (query block
+// descending), and within one query block the (b, h) pairs in order, so the
+// query heads sharing a K/V head run side by side.
 template <bool CAUSAL>
 __device__ __forceinline__ TileInfo tile_info(int tile, const FwdParams& p) {
     const int bh_count = p.B * p.Hq;
@@ -122,13 +127,24 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const FwdParams& p) {
     t.h = bh - t.b * p.Hq;
     t.hk = t.h / p.group;
     t.m0 = mb * kRowsPerTile;
-    int kv_end = p.Sk;
-    if (CAUSAL) {
-        const int last_row = min(t.m0 + kRowsPerTile - 1, p.Sq - 1);
-        kv_end = min(p.Sk, max(0, last_row + (p.Sk - p.Sq) + 1));
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        const int first = t.m0 + s * kBlockM;
+        const int last = min(first + kBlockM - 1, p.Sq - 1);
+        int kv_end = 0;
+        if (first < p.Sq) kv_end = CAUSAL ? min(p.Sk, max(0, last + (p.Sk - p.Sq) + 1)) : p.Sk;
+        t.nb[s] = (kv_end + kBlockN - 1) / kBlockN;
     }
-    t.n_blocks = (kv_end + kBlockN - 1) / kBlockN;
+    t.n = max(t.nb[0], t.nb[1]);
     return t;
+}
+
+// Persistent schedule: wave w hands CTA c the tile w*G + c for even w and
+// w*G + G-1-c for odd w (G = grid size). Walking the longest-first list in
+// this back-and-forth order pairs long tiles with short ones on each CTA.
+__device__ __forceinline__ int tile_of_wave(int w) {
+    const int G = gridDim.x;
+    return w * G + ((w & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
 }
 
 struct SyncCtx {
@@ -176,9 +192,11 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     uint32_t kv_fill = 0, q_loads = 0;
     bool alive = true;
-    for (int tile = blockIdx.x; tile < p.n_tiles && alive; tile += gridDim.x) {
+    for (int w = 0; w * (int)gridDim.x < p.n_tiles && alive; ++w) {
+        const int tile = tile_of_wave(w);
+        if (tile >= p.n_tiles) continue;
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
-        if (ti.n_blocks == 0) continue;
+        if (ti.n == 0) continue;
         if (q_loads > 0 && !wait_phase(bar(C::bQEmpty), (q_loads - 1) & 1u, sc)) { alive = false; break; }
         for (int t = 0; t < 2; ++t) {
             ptx::mbar_arrive_expect_tx(bar(C::bQFull + t), C::kTileBytes);
@@ -187,7 +205,7 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
                                  bar(C::bQFull + t), c * C::kBoxCols, ti.h, ti.m0 + t * kBlockM, ti.b);
         }
         ++q_loads;
-        for (int j = 0; j < ti.n_blocks && alive; ++j) {
+        for (int j = 0; j < ti.n && alive; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
                 const uint32_t slot = kv_fill % C::kSlots;
                 if (kv_fill >= (uint32_t)C::kSlots &&
@@ -276,9 +294,11 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
     };
 
     if (p.debug_stall) alive = wait_phase(bar(C::bStall), 0, sc);   // nothing ever arrives
-    for (int tile = blockIdx.x; tile < p.n_tiles && alive; tile += gridDim.x) {
+    for (int w = 0; w * (int)gridDim.x < p.n_tiles && alive; ++w) {
+        const int tile = tile_of_wave(w);
+        if (tile >= p.n_tiles) continue;
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
-        const int n = ti.n_blocks;
+        const int n = ti.n, n0 = ti.nb[0], n1 = ti.nb[1];     // n0, n1 are n or n - 1
         if (n == 0) continue;
         if (!wait_phase(bar(C::bQFull + 0), q_uses & 1u, sc) ||
             !wait_phase(bar(C::bQFull + 1), q_uses & 1u, sc)) { alive = false; break; }
@@ -286,26 +306,31 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         ptx::tc_fence_after_sync();
         uint32_t ks, vs;
         if (!acquire(ks)) { alive = false; break; }
-        issue_qk(0, ks);
-        issue_qk(1, ks);
+        if (n0 > 0) issue_qk(0, ks);
+        if (n1 > 0) issue_qk(1, ks);
         issued = true;
         ptx::tc_commit(bar(C::bKVEmpty + ks));
         if (n == 1) ptx::tc_commit(bar(C::bQEmpty));
         for (int j = 0; j < n; ++j) {
             const bool more = j + 1 < n;
-            if (!acquire(vs) || !wait_p(0)) { alive = false; break; }
-            issue_pv(0, vs, j > 0);
-            if (!more) ptx::tc_commit(bar(C::bOFull + 0));
+            if (!acquire(vs)) { alive = false; break; }
+            if (j < n0) {
+                if (!wait_p(0)) { alive = false; break; }
+                issue_pv(0, vs, j > 0);
+                if (j == n0 - 1) ptx::tc_commit(bar(C::bOFull + 0));
+            }
             if (more) {
                 if (!acquire(ks)) { alive = false; break; }
-                issue_qk(0, ks);
+                if (j + 1 < n0) issue_qk(0, ks);
             }
-            if (!wait_p(1)) { alive = false; break; }
-            issue_pv(1, vs, j > 0);
+            if (j < n1) {
+                if (!wait_p(1)) { alive = false; break; }
+                issue_pv(1, vs, j > 0);
+                if (j == n1 - 1) ptx::tc_commit(bar(C::bOFull + 1));
+            }
             ptx::tc_commit(bar(C::bKVEmpty + vs));
-            if (!more) ptx::tc_commit(bar(C::bOFull + 1));
             if (more) {
-                issue_qk(1, ks);
+                if (j + 1 < n1) issue_qk(1, ks);
                 ptx::tc_commit(bar(C::bKVEmpty + ks));
                 if (j + 1 == n - 1) ptx::tc_commit(bar(C::bQEmpty));
             }
@@ -333,13 +358,16 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
     constexpr float kLog2e = 1.4426950408889634f;
     uint32_t s_phase = 0, o_phase = 0;
 
-    for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x) {
+    for (int w = 0; w * (int)gridDim.x < p.n_tiles; ++w) {
+        const int tile = tile_of_wave(w);
+        if (tile >= p.n_tiles) continue;
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
+        const int nb = ti.nb[wg];
         const int row = ti.m0 + wg * kBlockM + r;
         const bool row_ok = row < p.Sq;
         uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (((size_t)ti.b * p.Sq + row) * p.Hq + ti.h) * D;
         float* lse_out = p.lse + ((size_t)ti.b * p.Hq + ti.h) * p.Sq + row;
-        if (ti.n_blocks == 0) {                               // no visible key anywhere in the tile
+        if (nb == 0) {                                        // no visible key for any row here
             if (row_ok) {
                 uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -358,7 +386,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
         float l_sum = 0.f;
         bool ok = true;
         const float sl = p.scale_log2;
-        for (int j = 0; j < ti.n_blocks; ++j) {
+        for (int j = 0; j < nb; ++j) {
             ok = wait_phase(bar(C::bSFull + wg), s_phase, sc);
             if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
             s_phase ^= 1u;
