@@ -89,13 +89,13 @@ struct TileCfg {
     static constexpr int bQFull = 0;        // [2]
     static constexpr int bQEmpty = 2;
     static constexpr int bSFull = 3;        // [2]
-    static constexpr int bPFull = 5;        // [2]
-    static constexpr int bOFull = 7;        // [2]
-    static constexpr int bDrain = 9;
-    static constexpr int bStall = 10;
-    static constexpr int bKVFull = 11;      // [kSlots]
-    static constexpr int bKVEmpty = 11 + kSlots;
-    static constexpr int kNumBars = 11 + 2 * kSlots;
+    static constexpr int bPFull = 5;        // [2][2]: P_t columns for keys 0-63 / 64-127 written
+    static constexpr int bOFull = 9;        // [2]
+    static constexpr int bDrain = 11;
+    static constexpr int bStall = 12;
+    static constexpr int bKVFull = 13;      // [kSlots]
+    static constexpr int bKVEmpty = 13 + kSlots;
+    static constexpr int kNumBars = 13 + 2 * kSlots;
     static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemUsed = kAbortOff + 4;
@@ -183,11 +183,19 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity, const
     }
 }
 
+// All 32 lanes wait on the same phase; the verdict is made warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const SyncCtx& sc) {
+    return __all_sync(0xffffffffu, wait_phase(bar, parity, sc));
+}
+
 // ------------------------------------------------------------ TMA producer
+// The whole warp runs this loop (so that addresses and coordinates stay
+// warp-uniform); lane 0 issues the copies.
 template <int D, bool CAUSAL>
 __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                          const FwdParams& p, uint32_t smem, const SyncCtx& sc) {
     using C = TileCfg<D>;
+    const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     uint32_t kv_fill = 0, q_loads = 0;
@@ -197,32 +205,36 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
         if (tile >= p.n_tiles) continue;
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
         if (ti.n == 0) continue;
-        if (q_loads > 0 && !wait_phase(bar(C::bQEmpty), (q_loads - 1) & 1u, sc)) { alive = false; break; }
-        for (int t = 0; t < 2; ++t) {
-            ptx::mbar_arrive_expect_tx(bar(C::bQFull + t), C::kTileBytes);
-            for (int c = 0; c < C::kBoxes; ++c)
-                ptx::tma_load_4d(smem + C::kQOff + t * C::kTileBytes + c * C::kBoxBytes, tmQ,
-                                 bar(C::bQFull + t), c * C::kBoxCols, ti.h, ti.m0 + t * kBlockM, ti.b);
+        if (q_loads > 0 && !warp_wait(bar(C::bQEmpty), (q_loads - 1) & 1u, sc)) { alive = false; break; }
+        if (leader) {
+            for (int t = 0; t < 2; ++t) {
+                ptx::mbar_arrive_expect_tx(bar(C::bQFull + t), C::kTileBytes);
+                for (int c = 0; c < C::kBoxes; ++c)
+                    ptx::tma_load_4d(smem + C::kQOff + t * C::kTileBytes + c * C::kBoxBytes, tmQ,
+                                     bar(C::bQFull + t), c * C::kBoxCols, ti.h, ti.m0 + t * kBlockM, ti.b);
+            }
         }
         ++q_loads;
         for (int j = 0; j < ti.n && alive; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
                 const uint32_t slot = kv_fill % C::kSlots;
                 if (kv_fill >= (uint32_t)C::kSlots &&
-                    !wait_phase(bar(C::bKVEmpty + slot), ((kv_fill / C::kSlots) - 1) & 1u, sc)) {
+                    !warp_wait(bar(C::bKVEmpty + slot), ((kv_fill / C::kSlots) - 1) & 1u, sc)) {
                     alive = false;
                     break;
                 }
-                ptx::mbar_arrive_expect_tx(bar(C::bKVFull + slot), C::kTileBytes);
-                const CUtensorMap* map = kv ? tmV : tmK;
-                for (int c = 0; c < C::kBoxes; ++c)
-                    ptx::tma_load_4d(smem + C::kKVOff + slot * C::kTileBytes + c * C::kBoxBytes, map,
-                                     bar(C::bKVFull + slot), c * C::kBoxCols, ti.hk, j * kBlockN, ti.b);
+                if (leader) {
+                    ptx::mbar_arrive_expect_tx(bar(C::bKVFull + slot), C::kTileBytes);
+                    const CUtensorMap* map = kv ? tmV : tmK;
+                    for (int c = 0; c < C::kBoxes; ++c)
+                        ptx::tma_load_4d(smem + C::kKVOff + slot * C::kTileBytes + c * C::kBoxBytes, map,
+                                         bar(C::bKVFull + slot), c * C::kBoxCols, ti.hk, j * kBlockN, ti.b);
+                }
                 ++kv_fill;
             }
         }
     }
-    // Shut down: wait until every copy this thread started has landed.
+    // Shut down: wait until every copy this warp started has landed.
     for (uint32_t s = 0; s < (uint32_t)C::kSlots; ++s) {
         if (kv_fill > s) {
             const uint32_t last = s + C::kSlots * ((kv_fill - 1 - s) / C::kSlots);
@@ -247,13 +259,20 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
 // first. Each commit covers every MMA issued before it, so "S_t ready" also
 // means that the previous O_t += P_t V has completed (the softmax may rescale
 // O_t and overwrite P_t after it).
+// The whole warp runs the loop with warp-uniform descriptors; lane 0 issues
+// every MMA and every commit (a commit covers the MMAs of its own thread).
 template <int D, bool CAUSAL, bool BF16>
 __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const SyncCtx& sc) {
     using C = TileCfg<D>;
+    const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     constexpr uint32_t kIdescQK = ptx::idesc_f16(128, kBlockN, BF16, false, false);
     constexpr uint32_t kIdescPV = ptx::idesc_f16(128, D, BF16, false, true);
+    // Base descriptors; a k-step advances the 16-byte-unit start address field.
+    const uint64_t q_desc0 = ptx::sdesc_kmajor_sw128(smem + C::kQOff);
+    const uint64_t kv_desc0 = ptx::sdesc_kmajor_sw128(smem + C::kKVOff);
+    const uint64_t v_desc0 = ptx::sdesc_mnmajor_sw128(smem + C::kKVOff, C::kBoxBytes);
     uint32_t kv_use = 0, q_uses = 0;
     uint32_t p_cnt[2] = {0, 0};
     bool issued = false;
@@ -261,47 +280,62 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
 
     auto acquire = [&](uint32_t& slot) -> bool {      // next K or V tile of the ring
         slot = kv_use % C::kSlots;
-        const bool ok = wait_phase(bar(C::bKVFull + slot), (kv_use / C::kSlots) & 1u, sc);
+        const bool ok = warp_wait(bar(C::bKVFull + slot), (kv_use / C::kSlots) & 1u, sc);
         ++kv_use;
         if (ok) ptx::tc_fence_after_sync();
         return ok;
     };
+    auto commit = [&](int b) {
+        if (leader) ptx::tc_commit(bar(b));
+    };
     auto issue_qk = [&](int t, uint32_t k_slot) {
-        const uint32_t q_base = smem + C::kQOff + t * C::kTileBytes;
-        const uint32_t k_base = smem + C::kKVOff + k_slot * C::kTileBytes;
+        const uint64_t qd = q_desc0 + (uint64_t)((t * C::kTileBytes) >> 4);
+        const uint64_t kd = kv_desc0 + (uint64_t)((k_slot * C::kTileBytes) >> 4);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-            ptx::mma_ss(tmem + C::s_col(t), ptx::sdesc_kmajor_sw128(q_base + off),
-                        ptx::sdesc_kmajor_sw128(k_base + off), kIdescQK, kk > 0 ? 1u : 0u);
-        }
-        ptx::tc_commit(bar(C::bSFull + t));
-    };
-    auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) {
-        const uint32_t v_base = smem + C::kKVOff + v_slot * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            ptx::mma_ts(tmem + C::kOCol0 + t * D, tmem + C::s_col(t) + kk * 8,
-                        ptx::sdesc_mnmajor_sw128(v_base + kk * 16 * 128, C::kBoxBytes), kIdescPV,
-                        (accumulate || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint64_t off = (uint64_t)((((kk >> 2) * C::kBoxBytes) + (kk & 3) * 32) >> 4);
+                ptx::mma_ss(tmem + C::s_col(t), qd + off, kd + off, kIdescQK, kk > 0 ? 1u : 0u);
+            }
+            ptx::tc_commit(bar(C::bSFull + t));
         }
     };
-    auto wait_p = [&](int t) -> bool {
-        const bool ok = wait_phase(bar(C::bPFull + t), p_cnt[t] & 1u, sc);
-        ++p_cnt[t];
+    // O_t += P_t V for the keys of one half of the block (8 columns of P per k-step).
+    auto issue_pv_half = [&](int t, uint32_t v_slot, int half, bool accumulate) {
+        const uint64_t vd = v_desc0 + (uint64_t)((v_slot * C::kTileBytes) >> 4);
+        if (leader) {
+#pragma unroll
+            for (int k4 = 0; k4 < kBlockN / 32; ++k4) {
+                const int kk = half * (kBlockN / 32) + k4;
+                ptx::mma_ts(tmem + C::kOCol0 + t * D, tmem + C::s_col(t) + kk * 8,
+                            vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+            }
+        }
+    };
+    auto wait_p = [&](int t, int half) -> bool {
+        const bool ok = warp_wait(bar(C::bPFull + 2 * t + half), p_cnt[t] & 1u, sc);
+        if (half == 1) ++p_cnt[t];
         if (ok) ptx::tc_fence_after_sync();
         return ok;
     };
+    // Each half of P_t is consumed as soon as the softmax has written it.
+    auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) -> bool {
+        if (!wait_p(t, 0)) return false;
+        issue_pv_half(t, v_slot, 0, accumulate);
+        if (!wait_p(t, 1)) return false;
+        issue_pv_half(t, v_slot, 1, accumulate);
+        return true;
+    };
 
-    if (p.debug_stall) alive = wait_phase(bar(C::bStall), 0, sc);   // nothing ever arrives
+    if (p.debug_stall) alive = warp_wait(bar(C::bStall), 0, sc);   // nothing ever arrives
     for (int w = 0; w * (int)gridDim.x < p.n_tiles && alive; ++w) {
         const int tile = tile_of_wave(w);
         if (tile >= p.n_tiles) continue;
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
         const int n = ti.n, n0 = ti.nb[0], n1 = ti.nb[1];     // n0, n1 are n or n - 1
         if (n == 0) continue;
-        if (!wait_phase(bar(C::bQFull + 0), q_uses & 1u, sc) ||
-            !wait_phase(bar(C::bQFull + 1), q_uses & 1u, sc)) { alive = false; break; }
+        if (!warp_wait(bar(C::bQFull + 0), q_uses & 1u, sc) ||
+            !warp_wait(bar(C::bQFull + 1), q_uses & 1u, sc)) { alive = false; break; }
         ++q_uses;
         ptx::tc_fence_after_sync();
         uint32_t ks, vs;
@@ -309,36 +343,34 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         if (n0 > 0) issue_qk(0, ks);
         if (n1 > 0) issue_qk(1, ks);
         issued = true;
-        ptx::tc_commit(bar(C::bKVEmpty + ks));
-        if (n == 1) ptx::tc_commit(bar(C::bQEmpty));
+        commit(C::bKVEmpty + ks);
+        if (n == 1) commit(C::bQEmpty);
         for (int j = 0; j < n; ++j) {
             const bool more = j + 1 < n;
             if (!acquire(vs)) { alive = false; break; }
             if (j < n0) {
-                if (!wait_p(0)) { alive = false; break; }
-                issue_pv(0, vs, j > 0);
-                if (j == n0 - 1) ptx::tc_commit(bar(C::bOFull + 0));
+                if (!issue_pv(0, vs, j > 0)) { alive = false; break; }
+                if (j == n0 - 1) commit(C::bOFull + 0);
             }
             if (more) {
                 if (!acquire(ks)) { alive = false; break; }
                 if (j + 1 < n0) issue_qk(0, ks);
             }
             if (j < n1) {
-                if (!wait_p(1)) { alive = false; break; }
-                issue_pv(1, vs, j > 0);
-                if (j == n1 - 1) ptx::tc_commit(bar(C::bOFull + 1));
+                if (!issue_pv(1, vs, j > 0)) { alive = false; break; }
+                if (j == n1 - 1) commit(C::bOFull + 1);
             }
-            ptx::tc_commit(bar(C::bKVEmpty + vs));
+            commit(C::bKVEmpty + vs);
             if (more) {
                 if (j + 1 < n1) issue_qk(1, ks);
-                ptx::tc_commit(bar(C::bKVEmpty + ks));
-                if (j + 1 == n - 1) ptx::tc_commit(bar(C::bQEmpty));
+                commit(C::bKVEmpty + ks);
+                if (j + 1 == n - 1) commit(C::bQEmpty);
             }
         }
     }
-    // Shut down: every MMA this thread issued must finish before TMEM is freed.
+    // Shut down: every MMA lane 0 issued must finish before TMEM is freed.
     if (issued) {
-        ptx::tc_commit(bar(C::bDrain));
+        commit(C::bDrain);
         drain_phase(bar(C::bDrain), 0, sc);
     }
 }
@@ -455,27 +487,6 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
                     m_used = m_new;
                 }
             }
-            const float nm = (m_used == -INFINITY) ? 0.f : -m_used;
-            uint32_t pk[kBlockN / 2];
-            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-            for (int c = 0; c < kBlockN / 2; ++c) {
-                float a, b;
-                if (ADDITIVE)
-                    ptx::add2(a, b, x[2 * c], x[2 * c + 1], nm, nm);
-                else
-                    ptx::fma2(a, b, x[2 * c], x[2 * c + 1], sl, sl, nm, nm);
-                a = ptx::ex2(a);
-                b = ptx::ex2(b);
-                if (c & 1)
-                    ptx::add2(l2, l3, l2, l3, a, b);
-                else
-                    ptx::add2(l0, l1, l0, l1, a, b);
-                pk[c] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
-            }
-            l_sum += (l0 + l1) + (l2 + l3);
-            ptx::tmem_st32(tS + 0, pk);
-            ptx::tmem_st32(tS + 32, pk + 32);
             if (rescale) {
                 // O_t holds the sum over the previous blocks and no product is
                 // running on it: "S_t ready" covered the previous O_t += P_t V.
@@ -490,9 +501,35 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
                     ptx::tmem_st32(tO + 32 * c, ov);
                 }
             }
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(bar(C::bPFull + wg));
+            const float nm = (m_used == -INFINITY) ? 0.f : -m_used;
+            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+            // P in two halves (keys 0-63, then 64-127); the product on the first
+            // half starts while the second half is being exponentiated.
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint32_t pk[kBlockN / 4];
+#pragma unroll
+                for (int c = 0; c < kBlockN / 4; ++c) {
+                    const int e = half * (kBlockN / 2) + 2 * c;
+                    float a, b;
+                    if (ADDITIVE)
+                        ptx::add2(a, b, x[e], x[e + 1], nm, nm);
+                    else
+                        ptx::fma2(a, b, x[e], x[e + 1], sl, sl, nm, nm);
+                    a = ptx::ex2(a);
+                    b = ptx::ex2(b);
+                    if (c & 1)
+                        ptx::add2(l2, l3, l2, l3, a, b);
+                    else
+                        ptx::add2(l0, l1, l0, l1, a, b);
+                    pk[c] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
+                }
+                ptx::tmem_st32(tS + half * 32, pk);
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before_sync();
+                ptx::mbar_arrive(bar(C::bPFull + 2 * wg + half));
+            }
+            l_sum += (l0 + l1) + (l2 + l3);
         }
         if (!ok) return;
         // ---- epilogue: O / l -> 16-bit, LSE -> FP32
@@ -546,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kTmaWarp && lane == 0) {
         const uint32_t bars = smem + C::kBarOff;
         for (int i = 0; i < C::kNumBars; ++i) {
-            const bool many = (i == C::bPFull || i == C::bPFull + 1);
+            const bool many = (i >= C::bPFull && i < C::bPFull + 4);
             ptx::mbar_init(bars + 8u * i, many ? kBlockM : 1u);
         }
         *abort_flag = 0u;
@@ -571,13 +608,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         role_softmax<D, CAUSAL, ADDITIVE, BF16>(p, smem, tmem, warp >> 2, sc);
     } else {
         ptx::setmaxnreg_dec<kControlRegs>();
-        if (warp == kMmaWarp) {
-            if (lane == 0) role_mma<D, CAUSAL, BF16>(p, smem, tmem, sc);
-            __syncwarp();
-        } else if (warp == kTmaWarp) {
-            if (lane == 0) role_tma<D, CAUSAL>(&tmQ, &tmK, &tmV, p, smem, sc);
-            __syncwarp();
-        }
+        if (warp == kMmaWarp)
+            role_mma<D, CAUSAL, BF16>(p, smem, tmem, sc);
+        else if (warp == kTmaWarp)
+            role_tma<D, CAUSAL>(&tmQ, &tmK, &tmV, p, smem, sc);
+        __syncwarp();
     }
 
     ptx::tc_fence_before_sync();
