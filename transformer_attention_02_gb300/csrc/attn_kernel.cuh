@@ -89,13 +89,13 @@ struct TileCfg {
     static constexpr int bQFull = 0;        // [2]
     static constexpr int bQEmpty = 2;
     static constexpr int bSFull = 3;        // [2]
-    static constexpr int bPFull = 5;        // [2][2]: P_t columns for keys 0-63 / 64-127 written
-    static constexpr int bOFull = 9;        // [2]
-    static constexpr int bDrain = 11;
-    static constexpr int bStall = 12;
-    static constexpr int bKVFull = 13;      // [kSlots]
-    static constexpr int bKVEmpty = 13 + kSlots;
-    static constexpr int kNumBars = 13 + 2 * kSlots;
+    static constexpr int bPFull = 5;        // [2]
+    static constexpr int bOFull = 7;        // [2]
+    static constexpr int bDrain = 9;
+    static constexpr int bStall = 10;
+    static constexpr int bKVFull = 11;      // [kSlots]
+    static constexpr int bKVEmpty = 11 + kSlots;
+    static constexpr int kNumBars = 11 + 2 * kSlots;
     static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemUsed = kAbortOff + 4;
@@ -300,31 +300,21 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
             ptx::tc_commit(bar(C::bSFull + t));
         }
     };
-    // O_t += P_t V for the keys of one half of the block (8 columns of P per k-step).
-    auto issue_pv_half = [&](int t, uint32_t v_slot, int half, bool accumulate) {
+    auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) {
         const uint64_t vd = v_desc0 + (uint64_t)((v_slot * C::kTileBytes) >> 4);
         if (leader) {
 #pragma unroll
-            for (int k4 = 0; k4 < kBlockN / 32; ++k4) {
-                const int kk = half * (kBlockN / 32) + k4;
+            for (int kk = 0; kk < kBlockN / 16; ++kk) {
                 ptx::mma_ts(tmem + C::kOCol0 + t * D, tmem + C::s_col(t) + kk * 8,
                             vd + (uint64_t)((kk * 16 * 128) >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
             }
         }
     };
-    auto wait_p = [&](int t, int half) -> bool {
-        const bool ok = warp_wait(bar(C::bPFull + 2 * t + half), p_cnt[t] & 1u, sc);
-        if (half == 1) ++p_cnt[t];
+    auto wait_p = [&](int t) -> bool {
+        const bool ok = warp_wait(bar(C::bPFull + t), p_cnt[t] & 1u, sc);
+        ++p_cnt[t];
         if (ok) ptx::tc_fence_after_sync();
         return ok;
-    };
-    // Each half of P_t is consumed as soon as the softmax has written it.
-    auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) -> bool {
-        if (!wait_p(t, 0)) return false;
-        issue_pv_half(t, v_slot, 0, accumulate);
-        if (!wait_p(t, 1)) return false;
-        issue_pv_half(t, v_slot, 1, accumulate);
-        return true;
     };
 
     if (p.debug_stall) alive = warp_wait(bar(C::bStall), 0, sc);   // nothing ever arrives
@@ -349,7 +339,8 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
             const bool more = j + 1 < n;
             if (!acquire(vs)) { alive = false; break; }
             if (j < n0) {
-                if (!issue_pv(0, vs, j > 0)) { alive = false; break; }
+                if (!wait_p(0)) { alive = false; break; }
+                issue_pv(0, vs, j > 0);
                 if (j == n0 - 1) commit(C::bOFull + 0);
             }
             if (more) {
@@ -357,7 +348,8 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
                 if (j + 1 < n0) issue_qk(0, ks);
             }
             if (j < n1) {
-                if (!issue_pv(1, vs, j > 0)) { alive = false; break; }
+                if (!wait_p(1)) { alive = false; break; }
+                issue_pv(1, vs, j > 0);
                 if (j == n1 - 1) commit(C::bOFull + 1);
             }
             commit(C::bKVEmpty + vs);
@@ -502,34 +494,29 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
                 }
             }
             const float nm = (m_used == -INFINITY) ? 0.f : -m_used;
+            uint32_t pk[kBlockN / 2];
             float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-            // P in two halves (keys 0-63, then 64-127); the product on the first
-            // half starts while the second half is being exponentiated.
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t pk[kBlockN / 4];
-#pragma unroll
-                for (int c = 0; c < kBlockN / 4; ++c) {
-                    const int e = half * (kBlockN / 2) + 2 * c;
-                    float a, b;
-                    if (ADDITIVE)
-                        ptx::add2(a, b, x[e], x[e + 1], nm, nm);
-                    else
-                        ptx::fma2(a, b, x[e], x[e + 1], sl, sl, nm, nm);
-                    a = ptx::ex2(a);
-                    b = ptx::ex2(b);
-                    if (c & 1)
-                        ptx::add2(l2, l3, l2, l3, a, b);
-                    else
-                        ptx::add2(l0, l1, l0, l1, a, b);
-                    pk[c] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
-                }
-                ptx::tmem_st32(tS + half * 32, pk);
-                ptx::tmem_st_wait();
-                ptx::tc_fence_before_sync();
-                ptx::mbar_arrive(bar(C::bPFull + 2 * wg + half));
+            for (int c = 0; c < kBlockN / 2; ++c) {
+                float a, b;
+                if (ADDITIVE)
+                    ptx::add2(a, b, x[2 * c], x[2 * c + 1], nm, nm);
+                else
+                    ptx::fma2(a, b, x[2 * c], x[2 * c + 1], sl, sl, nm, nm);
+                a = ptx::ex2(a);
+                b = ptx::ex2(b);
+                if (c & 1)
+                    ptx::add2(l2, l3, l2, l3, a, b);
+                else
+                    ptx::add2(l0, l1, l0, l1, a, b);
+                pk[c] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
             }
             l_sum += (l0 + l1) + (l2 + l3);
+            ptx::tmem_st32(tS + 0, pk);
+            ptx::tmem_st32(tS + 32, pk + 32);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before_sync();
+            ptx::mbar_arrive(bar(C::bPFull + wg));
         }
         if (!ok) return;
         // ---- epilogue: O / l -> 16-bit, LSE -> FP32
@@ -583,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kTmaWarp && lane == 0) {
         const uint32_t bars = smem + C::kBarOff;
         for (int i = 0; i < C::kNumBars; ++i) {
-            const bool many = (i >= C::bPFull && i < C::bPFull + 4);
+            const bool many = (i == C::bPFull || i == C::bPFull + 1);
             ptx::mbar_init(bars + 8u * i, many ? kBlockM : 1u);
         }
         *abort_flag = 0u;
