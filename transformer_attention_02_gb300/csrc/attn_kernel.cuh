@@ -253,6 +253,9 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
 // the other tile's two products):
 //     prologue:  S0 = Q0 K0^T, S1 = Q1 K0^T
 //     block j:   O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T
+// (K_{j+1} is acquired before the first product of block j, so that each
+// product pair is issued back to back: a wait between MMA groups lets the
+// tensor core's short queue run dry).
 // S_t and P_t share TMEM columns. The write of S_t for block j+1 is issued by
 // this thread after the product that reads P_t of block j, and the tensor core
 // executes the MMAs of one issuing thread in issue order, so that read happens
@@ -335,16 +338,17 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         issued = true;
         commit(C::bKVEmpty + ks);
         if (n == 1) commit(C::bQEmpty);
+        // Two groups of MMAs per block, each issued without a wait in between:
+        //   [O0 += P0 V_j, S0 = Q0 K_{j+1}^T]   [O1 += P1 V_j, S1 = Q1 K_{j+1}^T]
+        // Every wait happens while the tensor core still has queued work.
         for (int j = 0; j < n; ++j) {
             const bool more = j + 1 < n;
             if (!acquire(vs)) { alive = false; break; }
+            if (more && !acquire(ks)) { alive = false; break; }
             if (j < n0) {
                 if (!wait_p(0)) { alive = false; break; }
                 issue_pv(0, vs, j > 0);
                 if (j == n0 - 1) commit(C::bOFull + 0);
-            }
-            if (more) {
-                if (!acquire(ks)) { alive = false; break; }
                 if (j + 1 < n0) issue_qk(0, ks);
             }
             if (j < n1) {
