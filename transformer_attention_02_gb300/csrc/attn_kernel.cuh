@@ -20,8 +20,9 @@
 //   warps 0-3  softmax warpgroup 0: query rows [m0, m0+128)      (TMEM lanes 0-127)
 //   warps 4-7  softmax warpgroup 1: query rows [m0+128, m0+256)
 //   warp  8    MMA issuer (one thread) + TMEM allocation
-//   warp  9    TMA producer (one thread) + barrier initialisation
-//   warps 10-11 idle (they complete the third warpgroup for the register split)
+//   warp  9    TMA producer of K/V (one thread) + barrier initialisation
+//   warp 10    TMA producer of Q (one thread), a tile ahead for the lower sub-tile
+//   warp 11    idle (it completes the third warpgroup for the register split)
 // Pipelining ("ops-transformer：…实战" §2.3): while one warpgroup exponentiates
 // its scores, the tensor cores work on the other warpgroup's tile, and the TMA
 // warp streams the next K/V tiles into a ring of shared-memory slots.
@@ -59,6 +60,7 @@ struct FwdParams {
 constexpr int kThreads = 384;               // three warpgroups
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
+constexpr int kQWarp = 10;
 // Register split: launched at 168 per thread (384 x 168 = 64512), then the
 // softmax warpgroups grow to 200 and the MMA/TMA warpgroup shrinks to 104:
 // 128 x (200 + 200 + 104) = 64512. The host refuses to launch unless the
@@ -82,20 +84,23 @@ struct TileCfg {
     static constexpr int kBoxBytes = 128 * kBoxCols * 2;      // 128 rows x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;     // 128 rows x D
     static constexpr int kSlots = (D == 128) ? 4 : 8;         // K/V ring (K and V alternate)
+    // Q sub-tile buffers: the lower sub-tile alternates between buffers 0 and 1
+    // (so the next tile's is loaded a whole tile ahead), the upper uses buffer 2.
+    static constexpr int kQBufs = 3;
     static constexpr int kQOff = 0;
-    static constexpr int kKVOff = 2 * kTileBytes;
+    static constexpr int kKVOff = kQBufs * kTileBytes;
     static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
     // barrier indices
-    static constexpr int bQFull = 0;        // [2]
-    static constexpr int bQEmpty = 2;
-    static constexpr int bSFull = 3;        // [2]
-    static constexpr int bPFull = 5;        // [2]
-    static constexpr int bOFull = 7;        // [2]
-    static constexpr int bDrain = 9;
-    static constexpr int bStall = 10;
-    static constexpr int bKVFull = 11;      // [kSlots]
-    static constexpr int bKVEmpty = 11 + kSlots;
-    static constexpr int kNumBars = 11 + 2 * kSlots;
+    static constexpr int bQFull = 0;        // [kQBufs]
+    static constexpr int bQEmpty = 3;       // [kQBufs]
+    static constexpr int bSFull = 6;        // [2]
+    static constexpr int bPFull = 8;        // [2]
+    static constexpr int bOFull = 10;       // [2]
+    static constexpr int bDrain = 12;
+    static constexpr int bStall = 13;
+    static constexpr int bKVFull = 14;      // [kSlots]
+    static constexpr int bKVEmpty = 14 + kSlots;
+    static constexpr int kNumBars = 14 + 2 * kSlots;
     static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemUsed = kAbortOff + 4;
@@ -198,23 +203,13 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
     const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    uint32_t kv_fill = 0, q_loads = 0;
+    uint32_t kv_fill = 0;
     bool alive = true;
     for (int w = 0; w * (int)gridDim.x < p.n_tiles && alive; ++w) {
         const int tile = tile_of_wave(w);
         if (tile >= p.n_tiles) continue;
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
         if (ti.n == 0) continue;
-        if (q_loads > 0 && !warp_wait(bar(C::bQEmpty), (q_loads - 1) & 1u, sc)) { alive = false; break; }
-        if (leader) {
-            for (int t = 0; t < 2; ++t) {
-                ptx::mbar_arrive_expect_tx(bar(C::bQFull + t), C::kTileBytes);
-                for (int c = 0; c < C::kBoxes; ++c)
-                    ptx::tma_load_4d(smem + C::kQOff + t * C::kTileBytes + c * C::kBoxBytes, tmQ,
-                                     bar(C::bQFull + t), c * C::kBoxCols, ti.h, ti.m0 + t * kBlockM, ti.b);
-            }
-        }
-        ++q_loads;
         for (int j = 0; j < ti.n && alive; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
                 const uint32_t slot = kv_fill % C::kSlots;
@@ -241,10 +236,43 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
             drain_phase(bar(C::bKVFull + s), (last / C::kSlots) & 1u, sc);
         }
     }
-    if (q_loads > 0) {
-        drain_phase(bar(C::bQFull + 0), (q_loads - 1) & 1u, sc);
-        drain_phase(bar(C::bQFull + 1), (q_loads - 1) & 1u, sc);
+}
+
+// ------------------------------------------------------------- Q producer
+// Loads the Q sub-tiles of each work tile. The lower sub-tile alternates
+// between two buffers, so it is fetched as soon as the tile before the current
+// one has finished with it; the upper sub-tile reuses one buffer and is fetched
+// while the previous tile's last products and epilogue run.
+template <int D, bool CAUSAL>
+__device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t smem, const SyncCtx& sc) {
+    using C = TileCfg<D>;
+    const bool leader = (threadIdx.x & 31) == 0;
+    const uint32_t bars = smem + C::kBarOff;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    uint32_t uses[C::kQBufs] = {0, 0, 0};       // loads issued into each buffer
+    uint32_t nq = 0;                            // work tiles with at least one block
+    auto load = [&](int buf, int row0, const TileInfo& ti) -> bool {
+        if (uses[buf] > 0 && !warp_wait(bar(C::bQEmpty + buf), (uses[buf] - 1) & 1u, sc)) return false;
+        if (leader) {
+            ptx::mbar_arrive_expect_tx(bar(C::bQFull + buf), C::kTileBytes);
+            for (int c = 0; c < C::kBoxes; ++c)
+                ptx::tma_load_4d(smem + C::kQOff + buf * C::kTileBytes + c * C::kBoxBytes, tmQ,
+                                 bar(C::bQFull + buf), c * C::kBoxCols, ti.h, row0, ti.b);
+        }
+        ++uses[buf];
+        return true;
+    };
+    for (int w = 0; w * (int)gridDim.x < p.n_tiles; ++w) {
+        const int tile = tile_of_wave(w);
+        if (tile >= p.n_tiles) continue;
+        const TileInfo ti = tile_info<CAUSAL>(tile, p);
+        if (ti.n == 0) continue;
+        if (!load(nq & 1, ti.m0, ti) || !load(2, ti.m0 + kBlockM, ti)) break;
+        ++nq;
     }
+    // Shut down: wait until every copy this warp started has landed.
+    for (int b = 0; b < C::kQBufs; ++b)
+        if (uses[b] > 0) drain_phase(bar(C::bQFull + b), (uses[b] - 1) & 1u, sc);
 }
 
 // -------------------------------------------------------------- MMA issuer
@@ -253,9 +281,6 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
 // the other tile's two products):
 //     prologue:  S0 = Q0 K0^T, S1 = Q1 K0^T
 //     block j:   O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = Q1 K_{j+1}^T
-// (K_{j+1} is acquired before the first product of block j, so that each
-// product pair is issued back to back: a wait between MMA groups lets the
-// tensor core's short queue run dry).
 // S_t and P_t share TMEM columns. The write of S_t for block j+1 is issued by
 // this thread after the product that reads P_t of block j, and the tensor core
 // executes the MMAs of one issuing thread in issue order, so that read happens
@@ -274,9 +299,10 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
     constexpr uint32_t kIdescPV = ptx::idesc_f16(128, D, BF16, false, true);
     // Base descriptors; a k-step advances the 16-byte-unit start address field.
     const uint64_t q_desc0 = ptx::sdesc_kmajor_sw128(smem + C::kQOff);
+    uint32_t q_buf[2] = {0, 2};                  // Q buffers of the current tile's sub-tiles
     const uint64_t kv_desc0 = ptx::sdesc_kmajor_sw128(smem + C::kKVOff);
     const uint64_t v_desc0 = ptx::sdesc_mnmajor_sw128(smem + C::kKVOff, C::kBoxBytes);
-    uint32_t kv_use = 0, q_uses = 0;
+    uint32_t kv_use = 0, nq = 0;
     uint32_t p_cnt[2] = {0, 0};
     bool issued = false;
     bool alive = true;
@@ -292,7 +318,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         if (leader) ptx::tc_commit(bar(b));
     };
     auto issue_qk = [&](int t, uint32_t k_slot) {
-        const uint64_t qd = q_desc0 + (uint64_t)((t * C::kTileBytes) >> 4);
+        const uint64_t qd = q_desc0 + (uint64_t)((q_buf[t] * C::kTileBytes) >> 4);
         const uint64_t kd = kv_desc0 + (uint64_t)((k_slot * C::kTileBytes) >> 4);
         if (leader) {
 #pragma unroll
@@ -327,28 +353,34 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
         const int n = ti.n, n0 = ti.nb[0], n1 = ti.nb[1];     // n0, n1 are n or n - 1
         if (n == 0) continue;
-        if (!warp_wait(bar(C::bQFull + 0), q_uses & 1u, sc) ||
-            !warp_wait(bar(C::bQFull + 1), q_uses & 1u, sc)) { alive = false; break; }
-        ++q_uses;
-        ptx::tc_fence_after_sync();
+        // Q buffers of this tile: lower sub-tile in buffer nq & 1 (its (nq >> 1)-th
+        // use), upper sub-tile in buffer 2 (its nq-th use). Both phases are consumed
+        // even when a sub-tile has no block, to keep the parities in step.
+        q_buf[0] = nq & 1u;
+        auto release_q = [&]() {
+            commit(C::bQEmpty + q_buf[0]);
+            commit(C::bQEmpty + 2);
+        };
         uint32_t ks, vs;
-        if (!acquire(ks)) { alive = false; break; }
+        if (!warp_wait(bar(C::bQFull + q_buf[0]), (nq >> 1) & 1u, sc) || !acquire(ks)) { alive = false; break; }
         if (n0 > 0) issue_qk(0, ks);
-        if (n1 > 0) issue_qk(1, ks);
         issued = true;
+        if (!warp_wait(bar(C::bQFull + 2), nq & 1u, sc)) { alive = false; break; }
+        ptx::tc_fence_after_sync();
+        ++nq;
+        if (n1 > 0) issue_qk(1, ks);
         commit(C::bKVEmpty + ks);
-        if (n == 1) commit(C::bQEmpty);
-        // Two groups of MMAs per block, each issued without a wait in between:
-        //   [O0 += P0 V_j, S0 = Q0 K_{j+1}^T]   [O1 += P1 V_j, S1 = Q1 K_{j+1}^T]
-        // Every wait happens while the tensor core still has queued work.
+        if (n == 1) release_q();
         for (int j = 0; j < n; ++j) {
             const bool more = j + 1 < n;
             if (!acquire(vs)) { alive = false; break; }
-            if (more && !acquire(ks)) { alive = false; break; }
             if (j < n0) {
                 if (!wait_p(0)) { alive = false; break; }
                 issue_pv(0, vs, j > 0);
                 if (j == n0 - 1) commit(C::bOFull + 0);
+            }
+            if (more) {
+                if (!acquire(ks)) { alive = false; break; }
                 if (j + 1 < n0) issue_qk(0, ks);
             }
             if (j < n1) {
@@ -360,7 +392,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
             if (more) {
                 if (j + 1 < n1) issue_qk(1, ks);
                 commit(C::bKVEmpty + ks);
-                if (j + 1 == n - 1) commit(C::bQEmpty);
+                if (j + 1 == n - 1) release_q();
             }
         }
     }
@@ -529,17 +561,19 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
         o_phase ^= 1u;
         ptx::tc_fence_after_sync();
         const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
+        uint32_t ov[D];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) ptx::tmem_ld32(tO + 32 * c, ov + 32 * c);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) ptx::reg_fence32(ov + 32 * c);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            ptx::tmem_ld32(tO + 32 * c, ov);
-            ptx::tmem_ld_wait();
-            ptx::reg_fence32(ov);
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float a = __uint_as_float(ov[2 * i]) * inv_l;
-                const float b = __uint_as_float(ov[2 * i + 1]) * inv_l;
+                const float a = __uint_as_float(ov[32 * c + 2 * i]) * inv_l;
+                const float b = __uint_as_float(ov[32 * c + 2 * i + 1]) * inv_l;
                 w[i] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
             }
             if (row_ok) {
@@ -603,6 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             role_mma<D, CAUSAL, BF16>(p, smem, tmem, sc);
         else if (warp == kTmaWarp)
             role_tma<D, CAUSAL>(&tmQ, &tmK, &tmV, p, smem, sc);
+        else if (warp == kQWarp)
+            role_qload<D, CAUSAL>(&tmQ, p, smem, sc);
         __syncwarp();
     }
 
