@@ -142,3 +142,20 @@ def test_default_scale_is_inverse_sqrt_d():
     o1, l1 = run_gpu(q, k, v, None, False, scale=None)
     o2, l2 = run_gpu(q, k, v, None, False, scale=1.0 / math.sqrt(64))
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_output_aligned_to_16_but_not_32_bytes():
+    """O at an address that is 16-byte but not 32-byte aligned (the narrower store path)."""
+    cfg = _cfg(Sq=200, Sk=200)
+    q, k, v, _ = I.make_inputs(cfg)
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    ref_o, ref_l = A.attention(qd, kd, vd, causal=True)
+    buf = torch.zeros(qd.numel() + 16, dtype=torch.bfloat16, device=dev)
+    off = 8 if (buf.data_ptr() % 32 == 0) else 0          # 8 bf16 = 16 bytes
+    o = buf[off:off + qd.numel()].view(qd.shape)
+    assert o.data_ptr() % 16 == 0 and o.data_ptr() % 32 != 0
+    lse = torch.empty_like(ref_l)
+    A.attention(qd, kd, vd, causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ref_o) and torch.equal(lse, ref_l)

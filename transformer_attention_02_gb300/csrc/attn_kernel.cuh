@@ -52,6 +52,7 @@ struct FwdParams {
     int n_tiles;              // B * Hq * n_mblk
     float scale_log2;         // scale * log2(e)
     int mask_vec4;            // mask rows may be read with 16-byte loads
+    int o_vec8;               // O rows may be written with 32-byte stores
     int debug_stall;          // wait on a barrier nothing signals (timeout test)
     unsigned long long timeout_ns;
     unsigned int* status;     // device status word, bit 0 = a wait timed out
@@ -577,11 +578,16 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
                 w[i] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
             }
             if (row_ok) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-                dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                if (p.o_vec8) {
+                    ptx::st_global_v8(orow + 32 * c, w);
+                    ptx::st_global_v8(orow + 32 * c + 16, w + 8);
+                } else {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                }
             }
         }
         if (row_ok) *lse_out = l_sum > 0.f ? (m_used + log2f(l_sum)) * kLn2 : -INFINITY;

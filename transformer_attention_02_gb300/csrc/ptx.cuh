@@ -202,6 +202,13 @@ __device__ __forceinline__ void reg_fence32(uint32_t* r) {
 #undef ATTN_W8
 #undef ATTN_RW8
 
+// 32-byte vector store to global memory (the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 // Per-warpgroup register budget (all four warps of a warpgroup execute it).
 template <uint32_t kRegs>
 __device__ __forceinline__ void setmaxnreg_inc() {
