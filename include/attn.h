@@ -101,6 +101,17 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              float scale, int mask_kind, const float *mask, attn_stream_t stream);
 
 /*
+ * attn_fwd_f16 — the same operation with IEEE fp16 Q, K, V and O (FP32
+ * accumulation, FP32 running statistics, P rounded to fp16 for the second
+ * product, FP32 LSE). The pages run this operator in FP16 ([GUIDE] §5.1
+ * benchmark tensors, §8.2 "dtype": FP16). Arguments, layout, alignment,
+ * ownership and errors are exactly those of attn_fwd.
+ */
+int attn_fwd_f16(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                 float scale, int mask_kind, const float *mask, attn_stream_t stream);
+
+/*
  * attn_last_status — synchronises `stream`, then returns and clears the
  * current device's run-time status word: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT
  * if any launch since the last call gave up on a bounded wait (the kernel then

@@ -38,7 +38,8 @@ def check(o_gpu, lse_gpu, q, k, v, mask, mask_kind, *, scale=None, slices=None, 
     r0, r1 = (0, Sq) if rows is None else rows
     ref_o, ref_l = oracle.default().attention(
         I.bits(q), I.bits(k), I.bits(v), mask_kind=mask_kind,
-        mask=None if mask is None else mask.numpy(), scale=scale, slices=slices, rows=(r0, r1))
+        mask=None if mask is None else mask.numpy(), scale=scale, slices=slices, rows=(r0, r1),
+        dtype="f16" if q.dtype == torch.float16 else "bf16")
     og = o_gpu.float().cpu()
     lg = lse_gpu.float().cpu()
     got_o = np.stack([og[b, r0:r1, h, :].numpy() for b, h in slices]).astype(np.float64)

@@ -44,8 +44,9 @@ def lib() -> ctypes.CDLL:
             "(python -c 'import __graft_entry__ as g; g.build()')")
     L = ctypes.CDLL(path)
     P, I = ctypes.c_void_p, ctypes.c_int
-    L.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, P]
-    L.attn_fwd.restype = I
+    for f in (L.attn_fwd, L.attn_fwd_f16):
+        f.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, P]
+        f.restype = I
     L.attn_last_status.argtypes = [P]
     L.attn_last_status.restype = I
     L.attn_status_string.argtypes = [I]
@@ -64,6 +65,10 @@ def lib() -> ctypes.CDLL:
 
 def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, stream) -> int:
     return lib().attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, stream)
+
+
+def attn_fwd_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, stream) -> int:
+    return lib().attn_fwd_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, stream)
 
 
 def attn_last_status(stream) -> int:
@@ -96,15 +101,18 @@ def _stream_handle(stream):
 
 
 def attention(q, k, v, *, causal: bool = False, mask=None, scale=None, out=None, lse=None, stream=None):
-    """O, LSE = attention(Q, K, V) on (B, S, H, D) bf16 CUDA tensors.
+    """O, LSE = attention(Q, K, V) on (B, S, H, D) bf16 or fp16 CUDA tensors.
 
     mask: optional FP32 (B, Sq, Sk) additive mask (broadcast over heads).
     scale: None selects 1/sqrt(D). out/lse: optional preallocated outputs.
+    bf16 inputs go to attn_fwd, fp16 inputs to attn_fwd_f16.
     """
     import torch
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v must be bf16 or fp16")
     for name, t in (("q", q), ("k", k), ("v", v)):
-        if not (t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 4 and t.is_contiguous()):
-            raise ValueError(f"{name} must be a contiguous 4-D bf16 CUDA tensor (B, S, H, D)")
+        if not (t.is_cuda and t.dtype == q.dtype and t.dim() == 4 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor (B, S, H, D) of q's dtype")
     B, Sq, Hq, D = q.shape
     Bk, Sk, Hkv, Dk = k.shape
     if (Bk, Dk) != (B, D) or v.shape != k.shape:
@@ -121,8 +129,9 @@ def attention(q, k, v, *, causal: bool = False, mask=None, scale=None, out=None,
             raise ValueError("mask must be a contiguous FP32 CUDA tensor of shape (B, Sq, Sk)")
         mptr = mask.data_ptr()
     sc = float("nan") if scale is None else float(scale)
-    rc = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                  B, Hq, Hkv, Sq, Sk, D, sc, kind, mptr, _stream_handle(stream))
+    fn = attn_fwd if q.dtype == torch.bfloat16 else attn_fwd_f16
+    rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+            B, Hq, Hkv, Sq, Sk, D, sc, kind, mptr, _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc)
     return out, lse

@@ -22,7 +22,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 constexpr int kMaxDevices = 64;
 
@@ -208,6 +208,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              int Sk, int D, float scale, int mask_kind, const float* mask, attn_stream_t stream) {
     return attn_fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
                          reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                 int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, attn_stream_t stream) {
+    return attn_fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
+                         reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 int attn_last_status(attn_stream_t stream) {
