@@ -44,6 +44,8 @@
 #ifndef TRANSFORMER_ATTENTION_02_GB300_ATTN_H
 #define TRANSFORMER_ATTENTION_02_GB300_ATTN_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -110,6 +112,47 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
 int attn_fwd_f16(const void *q, const void *k, const void *v, void *o, float *lse,
                  int B, int Hq, int Hkv, int Sq, int Sk, int D,
                  float scale, int mask_kind, const float *mask, attn_stream_t stream);
+
+/*
+ * Split-key ("split-KV") variants, for few query rows against a long key/value
+ * sequence: decode and short prefill over a KV cache ("ATB orchestration blog"
+ * (hwcomputing.csdn.net/6a15a709662f9a54cb774da1) §四, FlashAttention with
+ * kv_cache; [GUIDE] §6.2, LLaMA/GPT with a KV cache; [MAP], ATB passes the KV
+ * cache in and out of FlashAttention). The keys are cut into `num_splits`
+ * contiguous ranges of whole 128-key blocks; each (b, h, 256-query-row, range)
+ * is one work tile of the fused kernel, which writes the range's FP32 output
+ * (normalised within the range) and its LSE ([OPS] §4.2 intermediate output)
+ * to the workspace; a second kernel merges the ranges:
+ *     lse = log sum_s exp(lse_s),   o = sum_s exp(lse_s - lse) o_s.
+ * The result equals attn_fwd's up to rounding.
+ *
+ *   num_splits  number of key ranges; 0 picks one (about 256 work tiles in
+ *               total, at most one range per 128-key block, at most 1024).
+ *               When the resolved count is 1 nothing is split and no
+ *               workspace is needed.
+ *   workspace   device scratch of at least attn_splitkv_workspace_bytes(...)
+ *               bytes, 256-byte aligned, owned by the caller; its contents are
+ *               overwritten. Two calls in flight at once need two workspaces.
+ *   workspace_bytes  its size.
+ * Other arguments and errors as for attn_fwd / attn_fwd_f16; a missing,
+ * misaligned or too small workspace is ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                     float scale, int mask_kind, const float *mask, int num_splits,
+                     void *workspace, size_t workspace_bytes, attn_stream_t stream);
+int attn_fwd_splitkv_f16(const void *q, const void *k, const void *v, void *o, float *lse,
+                         int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                         float scale, int mask_kind, const float *mask, int num_splits,
+                         void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/* attn_splitkv_num_splits — the number of key ranges attn_fwd_splitkv uses
+ * for these sizes (host only; 0 on invalid sizes). */
+int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk, int num_splits);
+
+/* attn_splitkv_workspace_bytes — workspace bytes attn_fwd_splitkv needs for
+ * these sizes (host only; 0 when nothing is split or the sizes are invalid). */
+size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int Sk, int D, int num_splits);
 
 /*
  * attn_last_status — synchronises `stream`, then returns and clears the

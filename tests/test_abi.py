@@ -97,3 +97,43 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(A, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         A.lib()
+
+
+# ------------------------------------------------------------ split keys (host only)
+
+def test_splitkv_range_count_and_workspace_size(lib):
+    # decode: B*Hq = 128 tiles -> two ranges give about 256 tiles
+    assert A.attn_splitkv_num_splits(4, 32, 1, 4096, 0) == 2
+    # explicit counts are capped by the number of 128-key blocks and made even-sized
+    assert A.attn_splitkv_num_splits(1, 8, 1, 1000, 3) == 3       # 8 blocks -> 3+3+2
+    assert A.attn_splitkv_num_splits(1, 8, 1, 1000, 100) == 8
+    assert A.attn_splitkv_num_splits(1, 8, 1, 1000, 5) == 4       # 2 blocks per range
+    assert A.attn_splitkv_num_splits(1, 8, 1, 0, 4) == 1          # no keys, no split
+    # a prefill with plenty of tiles is not split and needs no workspace
+    assert A.attn_splitkv_num_splits(4, 32, 2048, 2048, 0) == 1
+    assert A.attn_splitkv_workspace_bytes(4, 32, 2048, 2048, 128, 0) == 0
+    # workspace = FP32 O of every range, then (256-byte aligned) FP32 LSE of every range
+    rows = 4 * 32 * 1
+    o_bytes = 2 * rows * 128 * 4
+    assert A.attn_splitkv_workspace_bytes(4, 32, 1, 4096, 128, 0) == ((o_bytes + 255) // 256) * 256 + 2 * rows * 4
+    assert A.attn_splitkv_workspace_bytes(4, 32, 1, 4096, 96, 0) == 0   # unsupported head dim
+    assert A.attn_splitkv_num_splits(-1, 32, 1, 4096, 0) == 0
+
+
+def _call_split(num_splits=4, ws=P, ws_bytes=1 << 30, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, Hq=2, Hkv=2, Sq=16, Sk=4096, D=64, scale=0.0, kind=0, mask=None)
+    a.update(kw)
+    return A.attn_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["Sq"],
+                              a["Sk"], a["D"], a["scale"], a["kind"], a["mask"], num_splits, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_splits=-1), A.ATTN_ERR_INVALID_ARG),
+    (dict(ws=None), A.ATTN_ERR_INVALID_ARG),                 # a split needs a workspace
+    (dict(ws=P + 128), A.ATTN_ERR_INVALID_ARG),              # not 256-byte aligned
+    (dict(ws_bytes=64), A.ATTN_ERR_INVALID_ARG),             # too small
+    (dict(D=80), A.ATTN_ERR_UNSUPPORTED),
+    (dict(B=0), A.ATTN_OK),                                  # empty: nothing to do, no workspace needed
+])
+def test_splitkv_arguments_are_checked_before_launch(lib, kw, code):
+    assert _call_split(**kw) == code

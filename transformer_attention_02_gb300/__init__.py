@@ -7,4 +7,6 @@ seeded synthetic-input generator shared with the tests and the benchmark.
 from .attn import (  # noqa: F401
     ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_OK,
     MASK_ADDITIVE, MASK_CAUSAL, MASK_CAUSAL_ADDITIVE, MASK_NONE, AttnError, attention, attn_abi_version,
-    attn_debug_inject_stall, attn_fwd, attn_fwd_f16, attn_last_status, attn_set_wait_timeout_ns, attn_status_string)
+    attn_debug_inject_stall, attn_fwd, attn_fwd_f16, attn_fwd_splitkv, attn_fwd_splitkv_f16, attn_last_status,
+    attn_set_wait_timeout_ns, attn_splitkv_num_splits, attn_splitkv_workspace_bytes, attn_status_string,
+    attention_splitkv)

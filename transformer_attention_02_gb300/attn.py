@@ -47,6 +47,13 @@ def lib() -> ctypes.CDLL:
     for f in (L.attn_fwd, L.attn_fwd_f16):
         f.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, P]
         f.restype = I
+    for f in (L.attn_fwd_splitkv, L.attn_fwd_splitkv_f16):
+        f.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P, ctypes.c_size_t, P]
+        f.restype = I
+    L.attn_splitkv_num_splits.argtypes = [I, I, I, I, I]
+    L.attn_splitkv_num_splits.restype = I
+    L.attn_splitkv_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    L.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
     L.attn_last_status.argtypes = [P]
     L.attn_last_status.restype = I
     L.attn_status_string.argtypes = [I]
@@ -69,6 +76,26 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, str
 
 def attn_fwd_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, stream) -> int:
     return lib().attn_fwd_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, stream)
+
+
+def attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, num_splits,
+                     workspace, workspace_bytes, stream) -> int:
+    return lib().attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, num_splits,
+                                  workspace, workspace_bytes, stream)
+
+
+def attn_fwd_splitkv_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, num_splits,
+                         workspace, workspace_bytes, stream) -> int:
+    return lib().attn_fwd_splitkv_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, num_splits,
+                                      workspace, workspace_bytes, stream)
+
+
+def attn_splitkv_num_splits(B, Hq, Sq, Sk, num_splits=0) -> int:
+    return lib().attn_splitkv_num_splits(B, Hq, Sq, Sk, num_splits)
+
+
+def attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits=0) -> int:
+    return int(lib().attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits))
 
 
 def attn_last_status(stream) -> int:
@@ -134,4 +161,45 @@ def attention(q, k, v, *, causal: bool = False, mask=None, scale=None, out=None,
             B, Hq, Hkv, Sq, Sk, D, sc, kind, mptr, _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc)
+    return out, lse
+
+
+def attention_splitkv(q, k, v, *, causal: bool = False, mask=None, scale=None, num_splits: int = 0,
+                      workspace=None, out=None, lse=None, stream=None):
+    """attention() with the keys split into ranges that are merged afterwards.
+
+    workspace: optional uint8 CUDA tensor of at least attn_splitkv_workspace_bytes
+    bytes (allocated here with PyTorch when omitted).
+    """
+    import torch
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v must be bf16 or fp16")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (t.is_cuda and t.dtype == q.dtype and t.dim() == 4 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor (B, S, H, D) of q's dtype")
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or v.shape != k.shape:
+        raise ValueError("q, k, v shapes disagree")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    need = attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    kind = (MASK_CAUSAL if causal else MASK_NONE) + (MASK_ADDITIVE if mask is not None else 0)
+    mptr = None
+    if mask is not None:
+        if not (mask.is_cuda and mask.dtype == torch.float32 and mask.is_contiguous()
+                and tuple(mask.shape) == (B, Sq, Sk)):
+            raise ValueError("mask must be a contiguous FP32 CUDA tensor of shape (B, Sq, Sk)")
+        mptr = mask.data_ptr()
+    sc = float("nan") if scale is None else float(scale)
+    fn = attn_fwd_splitkv if q.dtype == torch.bfloat16 else attn_fwd_splitkv_f16
+    rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D,
+            sc, kind, mptr, int(num_splits), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_splitkv")
     return out, lse

@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -22,7 +23,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 constexpr int kMaxDevices = 64;
 
@@ -103,6 +104,54 @@ __global__ void fill_empty_rows_kernel(uint16_t* o, size_t n_o, float* lse, size
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_lse; i += stride) lse[i] = -INFINITY;
 }
 
+// Merge of the key ranges of a split computation, one warp per query row:
+//   lse = log sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s
+// where o_s is the softmax-weighted V of range s (normalised within the range).
+// A row whose ranges are all empty (lse_s = -inf) gets o = 0, lse = -inf.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __restrict__ o_part,
+                                                              const float* __restrict__ lse_part,
+                                                              uint16_t* __restrict__ o, float* __restrict__ lse,
+                                                              int n_splits, int B, int Hq, int Sq) {
+    constexpr int kPer = D / 32;                      // O elements per lane
+    const long long rows = (long long)B * Hq * Sq;
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    // row = (b * Hq + h) * Sq + i, the order of the partial buffers
+    const int i = (int)(row % Sq);
+    const long long bh = row / Sq;
+    const int h = (int)(bh % Hq);
+    const int b = (int)(bh / Hq);
+    float m = -INFINITY;
+    for (int s = lane; s < n_splits; s += 32) m = fmaxf(m, lse_part[(long long)s * rows + row]);
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+    float total = 0.f;
+    if (m != -INFINITY) {
+        for (int s = 0; s < n_splits; ++s) {
+            const float ls = lse_part[(long long)s * rows + row];
+            if (ls == -INFINITY) continue;
+            const float w = expf(ls - m);
+            total += w;
+            const float* src = o_part + ((long long)s * rows + row) * D + lane * kPer;
+#pragma unroll
+            for (int e = 0; e < kPer; ++e) acc[e] = fmaf(w, src[e], acc[e]);
+        }
+    }
+    const float inv = total > 0.f ? 1.f / total : 0.f;
+    uint16_t* dst = o + (((long long)b * Sq + i) * Hq + h) * D + lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2) {
+        const float a = acc[e] * inv, c = acc[e + 1] * inv;
+        const uint32_t packed = BF16 ? attn::ptx::pack_bf16x2(a, c) : attn::ptx::pack_f16x2(a, c);
+        *reinterpret_cast<uint32_t*>(dst + e) = packed;
+    }
+    if (lane == 0) lse[row] = total > 0.f ? m + logf(total) : -INFINITY;
+}
+
 template <int D, bool CAUSAL, bool ADDITIVE, bool BF16>
 int launch_one(DeviceInfo& dev, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const attn::FwdParams& p, int grid, cudaStream_t stream) {
@@ -135,9 +184,34 @@ int launch_d(DeviceInfo& dev, int mask_kind, const CUtensorMap& tq, const CUtens
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
 
+constexpr int kMaxSplits = 1024;
+constexpr size_t kWorkspaceAlign = 256;
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Number of key ranges for a split computation: the requested count, or (0)
+// enough to give about 256 work tiles; never more than there are 128-key
+// blocks, and every range holds the same number of blocks (the last may be short).
+int resolve_splits(int B, int Hq, int Sq, int Sk, int num_splits, int* split_blocks) {
+    const int n_kb = ceil_div(Sk, attn::kBlockN);
+    if (n_kb == 0) { *split_blocks = 1; return 1; }
+    long long base_tiles = (long long)B * Hq * ceil_div(Sq, attn::kRowsPerTile);
+    int want = num_splits > 0 ? num_splits : (int)std::max(1LL, (256 + base_tiles - 1) / std::max(1LL, base_tiles));
+    want = std::min(std::min(want, n_kb), kMaxSplits);
+    *split_blocks = ceil_div(n_kb, want);
+    return ceil_div(n_kb, *split_blocks);
+}
+
+size_t workspace_layout(int B, int Hq, int Sq, int D, int splits, size_t* lse_off) {
+    const size_t rows = (size_t)B * Hq * Sq;
+    const size_t o_bytes = (size_t)splits * rows * D * sizeof(float);
+    *lse_off = (o_bytes + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign;
+    return *lse_off + (size_t)splits * rows * sizeof(float);
+}
+
 int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                   int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, cudaStream_t stream,
-                  bool bf16) {
+                  bool bf16, int num_splits = 1, void* workspace = nullptr, size_t workspace_bytes = 0) {
     // ---- arguments (host only, nothing enqueued yet)
     if (B < 0 || Hq < 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_ADDITIVE) return ATTN_ERR_INVALID_ARG;
@@ -154,8 +228,16 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     if (additive && !aligned(mask, 4)) return ATTN_ERR_INVALID_ARG;
     if (Sq > (1 << 30) || Sk > (1 << 30)) return ATTN_ERR_INVALID_ARG;
     const long long n_mblk = ((long long)Sq + attn::kRowsPerTile - 1) / attn::kRowsPerTile;
-    if ((long long)B * Hq * n_mblk > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
+    int split_blocks = 1;
+    const int splits = resolve_splits(B, Hq, Sq, Sk, num_splits, &split_blocks);
+    if ((long long)B * Hq * n_mblk * splits > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     if (B == 0 || Hq == 0 || Sq == 0) return ATTN_OK;        // nothing to compute
+    size_t lse_off = 0;
+    if (splits > 1) {
+        if (!workspace || !aligned(workspace, kWorkspaceAlign)) return ATTN_ERR_INVALID_ARG;
+        if (workspace_bytes < workspace_layout(B, Hq, Sq, D, splits, &lse_off)) return ATTN_ERR_INVALID_ARG;
+    }
     if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt((float)D);
 
     DeviceInfo* dev = nullptr;
@@ -184,7 +266,13 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     p.Sk = Sk;
     p.group = Hq / Hkv;
     p.n_mblk = (int)n_mblk;
-    p.n_tiles = (int)((long long)B * Hq * n_mblk);
+    p.n_splits = splits;
+    p.split_blocks = splits > 1 ? split_blocks : ceil_div(Sk, attn::kBlockN);
+    p.n_tiles = (int)((long long)B * Hq * n_mblk * splits);
+    if (splits > 1) {
+        p.o_part = static_cast<float*>(workspace);
+        p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + lse_off);
+    }
     p.scale_log2 = scale * 1.4426950408889634f;
     p.mask_vec4 = additive && aligned(mask, 16) && (Sk % 4 == 0);
     p.o_vec8 = aligned(o, 32);
@@ -194,10 +282,25 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
 
     const int grid = p.n_tiles < dev->num_sms ? p.n_tiles : dev->num_sms;
     if (D == 128)
-        return bf16 ? launch_d<128, true>(*dev, mask_kind, tq, tk, tv, p, grid, stream)
-                    : launch_d<128, false>(*dev, mask_kind, tq, tk, tv, p, grid, stream);
-    return bf16 ? launch_d<64, true>(*dev, mask_kind, tq, tk, tv, p, grid, stream)
-                : launch_d<64, false>(*dev, mask_kind, tq, tk, tv, p, grid, stream);
+        rc = bf16 ? launch_d<128, true>(*dev, mask_kind, tq, tk, tv, p, grid, stream)
+                  : launch_d<128, false>(*dev, mask_kind, tq, tk, tv, p, grid, stream);
+    else
+        rc = bf16 ? launch_d<64, true>(*dev, mask_kind, tq, tk, tv, p, grid, stream)
+                  : launch_d<64, false>(*dev, mask_kind, tq, tk, tv, p, grid, stream);
+    if (rc != ATTN_OK || splits == 1) return rc;
+
+    // ---- merge the key ranges
+    const long long rows = (long long)B * Hq * Sq;
+    const unsigned blocks = (unsigned)((rows + 7) / 8);
+    auto* o16 = static_cast<uint16_t*>(o);
+    if (D == 128) {
+        if (bf16) splitkv_combine_kernel<128, true><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o16, lse, splits, B, Hq, Sq);
+        else splitkv_combine_kernel<128, false><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o16, lse, splits, B, Hq, Sq);
+    } else {
+        if (bf16) splitkv_combine_kernel<64, true><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o16, lse, splits, B, Hq, Sq);
+        else splitkv_combine_kernel<64, false><<<blocks, 256, 0, stream>>>(p.o_part, p.lse_part, o16, lse, splits, B, Hq, Sq);
+    }
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace
@@ -214,6 +317,35 @@ int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* ls
                  int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, attn_stream_t stream) {
     return attn_fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
                          reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int Sk, int D, int num_splits) {
+    if (B < 0 || Hq < 0 || Sq < 0 || Sk < 0 || (D != 64 && D != 128) || num_splits < 0) return 0;
+    int split_blocks = 1;
+    const int splits = resolve_splits(B, Hq, Sq, Sk, num_splits, &split_blocks);
+    if (splits <= 1) return 0;
+    size_t lse_off = 0;
+    return workspace_layout(B, Hq, Sq, D, splits, &lse_off);
+}
+
+int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk, int num_splits) {
+    if (B < 0 || Hq < 0 || Sq < 0 || Sk < 0 || num_splits < 0) return 0;
+    int split_blocks = 1;
+    return resolve_splits(B, Hq, Sq, Sk, num_splits, &split_blocks);
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, int num_splits,
+                     void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+    return attn_fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
+                         reinterpret_cast<cudaStream_t>(stream), true, num_splits, workspace, workspace_bytes);
+}
+
+int attn_fwd_splitkv_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                         int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, int num_splits,
+                         void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+    return attn_fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
+                         reinterpret_cast<cudaStream_t>(stream), false, num_splits, workspace, workspace_bytes);
 }
 
 int attn_last_status(attn_stream_t stream) {

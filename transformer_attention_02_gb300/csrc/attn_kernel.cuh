@@ -49,7 +49,11 @@ struct FwdParams {
     int B, Hq, Hkv, Sq, Sk;
     int group;                // Hq / Hkv
     int n_mblk;               // ceil(Sq / 256)
-    int n_tiles;              // B * Hq * n_mblk
+    int n_splits;             // key ranges per (b, h, query block); 1 = keys not split
+    int split_blocks;         // 128-key blocks per key range
+    int n_tiles;              // B * Hq * n_mblk * n_splits
+    float* o_part;            // split keys: FP32 O of each key range (n_splits, B, Hq, Sq, D), else null
+    float* lse_part;          // split keys: FP32 LSE of each key range (n_splits, B, Hq, Sq)
     float scale_log2;         // scale * log2(e)
     int mask_vec4;            // mask rows may be read with 16-byte loads
     int o_vec8;               // O rows may be written with 32-byte stores
@@ -115,6 +119,8 @@ struct TileCfg {
 
 struct TileInfo {
     int b, h, hk, m0;
+    int split;      // key range index
+    int kb0;        // first 128-key block of the key range
     int nb[2];      // KV blocks needed by query sub-tile t (rows m0+128t .. m0+128t+127)
     int n;          // max(nb[0], nb[1]): KV blocks streamed for the tile
 };
@@ -125,21 +131,28 @@ struct TileInfo {
 template <bool CAUSAL>
 __device__ __forceinline__ TileInfo tile_info(int tile, const FwdParams& p) {
     const int bh_count = p.B * p.Hq;
-    const int mb_rank = tile / bh_count;
-    const int bh = tile - mb_rank * bh_count;
+    const int per_mb = bh_count * p.n_splits;
+    const int mb_rank = tile / per_mb;
+    const int rem = tile - mb_rank * per_mb;
+    const int split = rem / bh_count;
+    const int bh = rem - split * bh_count;
     const int mb = CAUSAL ? (p.n_mblk - 1 - mb_rank) : mb_rank;
     TileInfo t;
     t.b = bh / p.Hq;
     t.h = bh - t.b * p.Hq;
     t.hk = t.h / p.group;
     t.m0 = mb * kRowsPerTile;
+    t.split = split;
+    t.kb0 = split * p.split_blocks;
+    const int range_begin = t.kb0 * kBlockN;
+    const int range_end = min(p.Sk, range_begin + p.split_blocks * kBlockN);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
         const int first = t.m0 + s * kBlockM;
         const int last = min(first + kBlockM - 1, p.Sq - 1);
-        int kv_end = 0;
-        if (first < p.Sq) kv_end = CAUSAL ? min(p.Sk, max(0, last + (p.Sk - p.Sq) + 1)) : p.Sk;
-        t.nb[s] = (kv_end + kBlockN - 1) / kBlockN;
+        int kv_end = range_begin;
+        if (first < p.Sq) kv_end = CAUSAL ? min(range_end, max(0, last + (p.Sk - p.Sq) + 1)) : range_end;
+        t.nb[s] = kv_end > range_begin ? (kv_end - range_begin + kBlockN - 1) / kBlockN : 0;
     }
     t.n = max(t.nb[0], t.nb[1]);
     return t;
@@ -224,7 +237,8 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
                     const CUtensorMap* map = kv ? tmV : tmK;
                     for (int c = 0; c < C::kBoxes; ++c)
                         ptx::tma_load_4d(smem + C::kKVOff + slot * C::kTileBytes + c * C::kBoxBytes, map,
-                                         bar(C::bKVFull + slot), c * C::kBoxCols, ti.hk, j * kBlockN, ti.b);
+                                         bar(C::bKVFull + slot), c * C::kBoxCols, ti.hk, (ti.kb0 + j) * kBlockN,
+                                         ti.b);
                 }
                 ++kv_fill;
             }
@@ -428,11 +442,21 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
         const bool row_ok = row < p.Sq;
         uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (((size_t)ti.b * p.Sq + row) * p.Hq + ti.h) * D;
         float* lse_out = p.lse + ((size_t)ti.b * p.Hq + ti.h) * p.Sq + row;
+        // With split keys this tile's result goes to the FP32 partial buffers.
+        const bool part = p.o_part != nullptr;
+        const size_t prow_index = (((size_t)ti.split * p.B + ti.b) * p.Hq + ti.h) * p.Sq + row;
+        float* prow = part ? p.o_part + prow_index * D : nullptr;
+        if (part) lse_out = p.lse_part + prow_index;
         if (nb == 0) {                                        // no visible key for any row here
             if (row_ok) {
                 uint4 z = make_uint4(0, 0, 0, 0);
+                if (part) {
 #pragma unroll
-                for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+                    for (int c = 0; c < D / 4; ++c) reinterpret_cast<uint4*>(prow)[c] = z;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+                }
                 *lse_out = -INFINITY;
             }
             continue;
@@ -459,7 +483,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
 #pragma unroll
             for (int c = 0; c < kBlockN / 32; ++c) ptx::reg_fence32(sr + 32 * c);
 
-            const int key0 = j * kBlockN;
+            const int key0 = (ti.kb0 + j) * kBlockN;
             const int vis = kv_lim - key0;                    // columns >= vis are hidden
             // x: raw scores, or (additive mask) logits in log2 units
             float x[kBlockN];
@@ -568,6 +592,16 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) ptx::reg_fence32(ov + 32 * c);
+        if (part) {
+            // FP32 O of this key range, normalised by its own sum (32-byte stores).
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__uint_as_float(ov[8 * c + i]) * inv_l);
+                if (row_ok) ptx::st_global_v8(prow + 8 * c, w);
+            }
+        } else {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
             uint32_t w[16];
@@ -589,6 +623,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
                     dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
                 }
             }
+        }
         }
         if (row_ok) *lse_out = l_sum > 0.f ? (m_used + log2f(l_sum)) * kLn2 : -INFINITY;
     }
