@@ -126,8 +126,10 @@ int attn_fwd_f16(const void *q, const void *k, const void *v, void *o, float *ls
  *     lse = log sum_s exp(lse_s),   o = sum_s exp(lse_s - lse) o_s.
  * The result equals attn_fwd's up to rounding.
  *
- *   num_splits  number of key ranges; 0 picks one (about 256 work tiles in
- *               total, at most one range per 128-key block, at most 1024).
+ *   num_splits  number of key ranges; 0 picks as many as fill one wave of
+ *               work tiles on the current device's SMs (1 when the unsplit
+ *               tiles already cover them); at most one range per 128-key
+ *               block, at most 1024.
  *               When the resolved count is 1 nothing is split and no
  *               workspace is needed.
  *   workspace   device scratch of at least attn_splitkv_workspace_bytes(...)
@@ -147,11 +149,12 @@ int attn_fwd_splitkv_f16(const void *q, const void *k, const void *v, void *o, f
                          void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /* attn_splitkv_num_splits — the number of key ranges attn_fwd_splitkv uses
- * for these sizes (host only; 0 on invalid sizes). */
+ * for these sizes on the current device (host only; 0 on invalid sizes). */
 int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk, int num_splits);
 
 /* attn_splitkv_workspace_bytes — workspace bytes attn_fwd_splitkv needs for
- * these sizes (host only; 0 when nothing is split or the sizes are invalid). */
+ * these sizes on the current device (host only; 0 when nothing is split or
+ * the sizes are invalid). */
 size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int Sk, int D, int num_splits);
 
 /*

@@ -102,8 +102,9 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 # ------------------------------------------------------------ split keys (host only)
 
 def test_splitkv_range_count_and_workspace_size(lib):
-    # decode: B*Hq = 128 tiles -> two ranges give about 256 tiles
-    assert A.attn_splitkv_num_splits(4, 32, 1, 4096, 0) == 2
+    # automatic choice without a GPU (148 SMs assumed): fill one wave of tiles
+    assert A.attn_splitkv_num_splits(1, 16, 1, 8192, 0) == 8      # 16 tiles: 9 wanted, 64 blocks -> 8 x 8
+    assert A.attn_splitkv_num_splits(4, 32, 1, 4096, 0) == 1      # 128 tiles already: no split
     # explicit counts are capped by the number of 128-key blocks and made even-sized
     assert A.attn_splitkv_num_splits(1, 8, 1, 1000, 3) == 3       # 8 blocks -> 3+3+2
     assert A.attn_splitkv_num_splits(1, 8, 1, 1000, 100) == 8
@@ -115,8 +116,8 @@ def test_splitkv_range_count_and_workspace_size(lib):
     # workspace = FP32 O of every range, then (256-byte aligned) FP32 LSE of every range
     rows = 4 * 32 * 1
     o_bytes = 2 * rows * 128 * 4
-    assert A.attn_splitkv_workspace_bytes(4, 32, 1, 4096, 128, 0) == ((o_bytes + 255) // 256) * 256 + 2 * rows * 4
-    assert A.attn_splitkv_workspace_bytes(4, 32, 1, 4096, 96, 0) == 0   # unsupported head dim
+    assert A.attn_splitkv_workspace_bytes(4, 32, 1, 4096, 128, 2) == ((o_bytes + 255) // 256) * 256 + 2 * rows * 4
+    assert A.attn_splitkv_workspace_bytes(4, 32, 1, 4096, 96, 2) == 0   # unsupported head dim
     assert A.attn_splitkv_num_splits(-1, 32, 1, 4096, 0) == 0
 
 

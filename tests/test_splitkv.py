@@ -13,11 +13,12 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     # B, Hq, Hkv, Sq, Sk, D, mask kind, num_splits
-    (4, 32, 8, 1, 4096, 128, 1, 0),        # GQA decode, automatic split
+    (1, 16, 4, 1, 8192, 128, 1, 0),        # GQA decode, automatic split
     (2, 8, 8, 16, 8192, 64, 1, 0),
     (1, 8, 1, 1, 1000, 128, 0, 3),         # MQA, ragged ranges 3+3+2 blocks
     (1, 4, 2, 200, 1000, 128, 3, 4),       # causal + additive, some ranges empty for early rows
-    (1, 2, 2, 300, 100, 64, 1, 2),         # Sq > Sk: rows with no key at all
+    (1, 2, 2, 400, 300, 64, 1, 2),         # Sq > Sk: rows with no key at all
+    (4, 32, 8, 1, 4096, 128, 1, 2),        # batched GQA decode, two ranges
     (2, 4, 4, 64, 2100, 128, 2, 7),
 ]
 

@@ -189,14 +189,28 @@ constexpr size_t kWorkspaceAlign = 256;
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
+// SM count of the current device (148 when it cannot be read, e.g. no GPU).
+int current_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+        cudaGetLastError();
+        return 148;
+    }
+    return sms;
+}
+
 // Number of key ranges for a split computation: the requested count, or (0)
-// enough to give about 256 work tiles; never more than there are 128-key
-// blocks, and every range holds the same number of blocks (the last may be short).
+// as many as fill one wave of work tiles on the device's SMs without
+// exceeding it (1 when the unsplit tiles already cover every SM); never more
+// than there are 128-key blocks, and every range holds the same number of
+// blocks (the last may be short).
 int resolve_splits(int B, int Hq, int Sq, int Sk, int num_splits, int* split_blocks) {
     const int n_kb = ceil_div(Sk, attn::kBlockN);
     if (n_kb == 0) { *split_blocks = 1; return 1; }
-    long long base_tiles = (long long)B * Hq * ceil_div(Sq, attn::kRowsPerTile);
-    int want = num_splits > 0 ? num_splits : (int)std::max(1LL, (256 + base_tiles - 1) / std::max(1LL, base_tiles));
+    const long long base_tiles = std::max(1LL, (long long)B * Hq * ceil_div(Sq, attn::kRowsPerTile));
+    int want = num_splits;
+    if (want == 0) want = num_splits == 0 && base_tiles < current_sm_count() ? (int)(current_sm_count() / base_tiles) : 1;
     want = std::min(std::min(want, n_kb), kMaxSplits);
     *split_blocks = ceil_div(n_kb, want);
     return ceil_div(n_kb, *split_blocks);
