@@ -158,6 +158,35 @@ int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk, int num_splits);
 size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int Sk, int D, int num_splits);
 
 /*
+ * attn_fwd_splitkv_noalloc — attn_fwd_splitkv (bf16) for callers that cannot
+ * allocate device memory: for example a plug-in running inside a host
+ * framework that owns all device memory and forbids allocations after start-up,
+ * or a latency-critical path that must not pay for (or synchronise on)
+ * cudaMalloc. It takes no workspace: the partial results live in a fixed
+ * 32 MiB array in the library's own device memory (a static __device__
+ * array, present on every GPU that loads the library until the process exits).
+ * The pages have no counterpart; this entry point exists only for such callers.
+ *
+ *   Arguments, layout, results and errors as for attn_fwd_splitkv.
+ *   Limit: attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits) must not
+ *   exceed 32 MiB (33554432 bytes); larger problems are refused with
+ *   ATTN_ERR_UNSUPPORTED before anything is launched.
+ *   The first call on each device looks up the array's device address on that
+ *   device (cudaGetSymbolAddress, which may synchronise); make that first call
+ *   before any stream capture.
+ *   All calls on a device share the one array and it keeps the last call's
+ *   contents. Nothing in it needs to start at zero (every partial result is
+ *   written before it is read), but calls whose work overlaps on the GPU (for
+ *   example on two streams at once) race on it: serialise them.
+ *   The call itself allocates nothing: no cudaMalloc, no cudaFree, no
+ *   allocating library routine.
+ */
+int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                             float scale, int mask_kind, const float *mask, int num_splits,
+                             attn_stream_t stream);
+
+/*
  * attn_last_status — synchronises `stream`, then returns and clears the
  * current device's run-time status word: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT
  * if any launch since the last call gave up on a bounded wait (the kernel then

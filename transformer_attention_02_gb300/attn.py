@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
     for f in (L.attn_fwd_splitkv, L.attn_fwd_splitkv_f16):
         f.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P, ctypes.c_size_t, P]
         f.restype = I
+    L.attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]
+    L.attn_fwd_splitkv_noalloc.restype = I
     L.attn_splitkv_num_splits.argtypes = [I, I, I, I, I]
     L.attn_splitkv_num_splits.restype = I
     L.attn_splitkv_workspace_bytes.argtypes = [I, I, I, I, I, I]
@@ -88,6 +90,13 @@ def attn_fwd_splitkv_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kin
                          workspace, workspace_bytes, stream) -> int:
     return lib().attn_fwd_splitkv_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, num_splits,
                                       workspace, workspace_bytes, stream)
+
+
+def attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, num_splits,
+                             stream) -> int:
+    """The allocation-free split-key entry point (bf16): its scratch is the library's fixed 32 MiB array."""
+    return lib().attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
+                                          num_splits, stream)
 
 
 def attn_splitkv_num_splits(B, Hq, Sq, Sk, num_splits=0) -> int:

@@ -362,6 +362,54 @@ int attn_fwd_splitkv_f16(const void* q, const void* k, const void* v, void* o, f
                          reinterpret_cast<cudaStream_t>(stream), false, num_splits, workspace, workspace_bytes);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Scratch for attn_fwd_splitkv_noalloc: one fixed array per device that loads
+// this library, held until the process exits, shared by every call.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+void* g_noalloc_scratch_ptr[kMaxDevices] = {};   // device address per device, guarded by g_mutex
+
+// Device address of the scratch array on the current device. In host code the
+// array's name is only a host-side stand-in, so its address must come from
+// cudaGetSymbolAddress, once per device, with that device current.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_noalloc_scratch_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return ATTN_ERR_CUDA;
+        g_noalloc_scratch_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_scratch_ptr[dev];
+    return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                             int Hkv, int Sq, int Sk, int D, float scale, int mask_kind, const float* mask,
+                             int num_splits, attn_stream_t stream) {
+    // Refuse, before anything else, a problem whose partial results would not
+    // fit in the fixed scratch array.
+    if (attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits) > kNoAllocScratchBytes)
+        return ATTN_ERR_UNSUPPORTED;
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != ATTN_OK) return rc;
+    void* scratch = nullptr;
+    rc = noalloc_scratch(&scratch);
+    if (rc != ATTN_OK) return rc;
+    return attn_fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
+                         reinterpret_cast<cudaStream_t>(stream), true, num_splits, scratch, kNoAllocScratchBytes);
+}
+
 int attn_last_status(attn_stream_t stream) {
     DeviceInfo* dev = nullptr;
     int rc = device_info(&dev);
