@@ -472,8 +472,9 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
         bool ok = true;
         const float sl = p.scale_log2;
         for (int j = 0; j < nb; ++j) {
-            ok = wait_phase(bar(C::bSFull + wg), s_phase, sc);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+            // Warpgroup-uniform verdict: the named barriers below need all four warps.
+            ok = ptx::named_barrier_and(1 + wg, kBlockM, wait_phase(bar(C::bSFull + wg), s_phase, sc));
+            if (!ok) break;
             s_phase ^= 1u;
             ptx::tc_fence_after_sync();
             uint32_t sr[kBlockN];
@@ -577,12 +578,15 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
             ptx::tmem_st32(tS + 32, pk + 32);
             ptx::tmem_st_wait();
             ptx::tc_fence_before_sync();
-            ptx::mbar_arrive(bar(C::bPFull + wg));
+            // All 128 rows of P_t are in TMEM once the warpgroup has met; one
+            // thread then tells the MMA issuer (one arrival instead of 128).
+            ptx::named_barrier_sync(1 + wg, kBlockM);
+            if (r == 0) ptx::mbar_arrive(bar(C::bPFull + wg));
         }
         if (!ok) return;
         // ---- epilogue: O / l -> 16-bit, LSE -> FP32
-        ok = wait_phase(bar(C::bOFull + wg), o_phase, sc);
-        if (!__all_sync(0xffffffffu, ok)) return;
+        ok = ptx::named_barrier_and(1 + wg, kBlockM, wait_phase(bar(C::bOFull + wg), o_phase, sc));
+        if (!ok) return;
         o_phase ^= 1u;
         ptx::tc_fence_after_sync();
         const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -649,8 +653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kTmaWarp && lane == 0) {
         const uint32_t bars = smem + C::kBarOff;
         for (int i = 0; i < C::kNumBars; ++i) {
-            const bool many = (i == C::bPFull || i == C::bPFull + 1);
-            ptx::mbar_init(bars + 8u * i, many ? kBlockM : 1u);
+            ptx::mbar_init(bars + 8u * i, 1u);
         }
         *abort_flag = 0u;
         ptx::fence_barrier_init();
