@@ -88,11 +88,7 @@ struct TileCfg {
     static constexpr int kBoxes = D / kBoxCols;
     static constexpr int kBoxBytes = 128 * kBoxCols * 2;      // 128 rows x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;     // 128 rows x D
-    static constexpr int kSlots = (D == 128) ? 4 : 8;         // K/V tile slots
-    // The ring moves in stages of two slots: stage (V_j, K_{j+1}) holds what
-    // the MMA issuer needs in block j (the last V_{n-1} of a tile is paired with
-    // the next tile's K_0); the first stage of the kernel holds K_0 alone.
-    static constexpr int kStages = kSlots / 2;
+    static constexpr int kSlots = (D == 128) ? 4 : 8;         // K/V ring (K and V alternate)
     // Q sub-tile buffers: the lower sub-tile alternates between buffers 0 and 1
     // (so the next tile's is loaded a whole tile ahead), the upper uses buffer 2.
     static constexpr int kQBufs = 3;
@@ -107,9 +103,9 @@ struct TileCfg {
     static constexpr int bOFull = 10;       // [2]
     static constexpr int bDrain = 12;
     static constexpr int bStall = 13;
-    static constexpr int bKVFull = 14;      // [kStages]
-    static constexpr int bKVEmpty = 14 + kStages;
-    static constexpr int kNumBars = 14 + 2 * kStages;
+    static constexpr int bKVFull = 14;      // [kSlots]
+    static constexpr int bKVEmpty = 14 + kSlots;
+    static constexpr int kNumBars = 14 + 2 * kSlots;
     static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemUsed = kAbortOff + 4;
@@ -221,57 +217,38 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
     const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    uint32_t g = 0;              // stages begun
-    uint32_t st = 0;             // current stage
-    bool open = false;           // current stage still waits for its K half
+    uint32_t kv_fill = 0;
     bool alive = true;
-    auto begin_stage = [&]() -> bool {
-        st = g % C::kStages;
-        if (g >= (uint32_t)C::kStages && !warp_wait(bar(C::bKVEmpty + st), ((g / C::kStages) - 1) & 1u, sc))
-            return false;
-        ++g;
-        open = true;
-        return true;
-    };
-    auto load = [&](const CUtensorMap* map, int slot, const TileInfo& ti, int j) {
-        for (int c = 0; c < C::kBoxes; ++c)
-            ptx::tma_load_4d(smem + C::kKVOff + slot * C::kTileBytes + c * C::kBoxBytes, map, bar(C::bKVFull + st),
-                             c * C::kBoxCols, ti.hk, (ti.kb0 + j) * kBlockN, ti.b);
-    };
-    auto load_v = [&](const TileInfo& ti, int j) {             // expected, not yet arrived
-        if (leader) {
-            ptx::mbar_expect_tx(bar(C::bKVFull + st), C::kTileBytes);
-            load(tmV, 2 * st + 1, ti, j);
-        }
-    };
-    auto load_k = [&](const TileInfo& ti, int j) {             // completes the stage
-        if (leader) {
-            ptx::mbar_arrive_expect_tx(bar(C::bKVFull + st), C::kTileBytes);
-            load(tmK, 2 * st, ti, j);
-        }
-        open = false;
-    };
     for (int w = 0; w * (int)gridDim.x < p.n_tiles && alive; ++w) {
         const int tile = tile_of_wave(w);
         if (tile >= p.n_tiles) continue;
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
         if (ti.n == 0) continue;
-        if (!open && !begin_stage()) { alive = false; break; }   // the first tile: K_0 alone
-        load_k(ti, 0);
-        for (int j = 0; j < ti.n; ++j) {
-            if (!begin_stage()) { alive = false; break; }
-            load_v(ti, j);
-            if (j + 1 < ti.n) load_k(ti, j + 1);                   // else the next tile's K_0 completes it
+        for (int j = 0; j < ti.n && alive; ++j) {
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint32_t slot = kv_fill % C::kSlots;
+                if (kv_fill >= (uint32_t)C::kSlots &&
+                    !warp_wait(bar(C::bKVEmpty + slot), ((kv_fill / C::kSlots) - 1) & 1u, sc)) {
+                    alive = false;
+                    break;
+                }
+                if (leader) {
+                    ptx::mbar_arrive_expect_tx(bar(C::bKVFull + slot), C::kTileBytes);
+                    const CUtensorMap* map = kv ? tmV : tmK;
+                    for (int c = 0; c < C::kBoxes; ++c)
+                        ptx::tma_load_4d(smem + C::kKVOff + slot * C::kTileBytes + c * C::kBoxBytes, map,
+                                         bar(C::bKVFull + slot), c * C::kBoxCols, ti.hk, (ti.kb0 + j) * kBlockN,
+                                         ti.b);
+                }
+                ++kv_fill;
+            }
         }
     }
-    // Shut down: close a stage still waiting for a K half, then wait until
-    // every copy this warp started has landed.
-    if (open && leader) ptx::mbar_arrive(bar(C::bKVFull + st));
-    __syncwarp();
-    for (uint32_t s2 = 0; s2 < (uint32_t)C::kStages; ++s2) {
-        if (g > s2) {
-            const uint32_t last = s2 + C::kStages * ((g - 1 - s2) / C::kStages);
-            drain_phase(bar(C::bKVFull + s2), (last / C::kStages) & 1u, sc);
+    // Shut down: wait until every copy this warp started has landed.
+    for (uint32_t s = 0; s < (uint32_t)C::kSlots; ++s) {
+        if (kv_fill > s) {
+            const uint32_t last = s + C::kSlots * ((kv_fill - 1 - s) / C::kSlots);
+            drain_phase(bar(C::bKVFull + s), (last / C::kSlots) & 1u, sc);
         }
     }
 }
@@ -341,15 +318,13 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
     const uint64_t kv_desc0 = ptx::sdesc_kmajor_sw128(smem + C::kKVOff);
     const uint64_t v_desc0 = ptx::sdesc_mnmajor_sw128(smem + C::kKVOff, C::kBoxBytes);
     uint32_t kv_use = 0, nq = 0;
-    uint32_t k0_stage = 0;                        // stage holding the next tile's K_0
-    bool have_k0 = false;
     uint32_t p_cnt[2] = {0, 0};
     bool issued = false;
     bool alive = true;
 
-    auto acquire = [&](uint32_t& stage) -> bool {     // next stage of the ring
-        stage = kv_use % C::kStages;
-        const bool ok = warp_wait(bar(C::bKVFull + stage), (kv_use / C::kStages) & 1u, sc);
+    auto acquire = [&](uint32_t& slot) -> bool {      // next K or V tile of the ring
+        slot = kv_use % C::kSlots;
+        const bool ok = warp_wait(bar(C::bKVFull + slot), (kv_use / C::kSlots) & 1u, sc);
         ++kv_use;
         if (ok) ptx::tc_fence_after_sync();
         return ok;
@@ -359,7 +334,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
     };
     auto issue_qk = [&](int t, uint32_t k_slot) {
         const uint64_t qd = q_desc0 + (uint64_t)((q_buf[t] * C::kTileBytes) >> 4);
-        const uint64_t kd = kv_desc0 + (uint64_t)((2 * k_slot * C::kTileBytes) >> 4);   // K half of the stage
+        const uint64_t kd = kv_desc0 + (uint64_t)((k_slot * C::kTileBytes) >> 4);
         if (leader) {
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -370,7 +345,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         }
     };
     auto issue_pv = [&](int t, uint32_t v_slot, bool accumulate) {
-        const uint64_t vd = v_desc0 + (uint64_t)(((2 * v_slot + 1) * C::kTileBytes) >> 4);   // V half
+        const uint64_t vd = v_desc0 + (uint64_t)((v_slot * C::kTileBytes) >> 4);
         if (leader) {
 #pragma unroll
             for (int kk = 0; kk < kBlockN / 16; ++kk) {
@@ -401,41 +376,38 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
             commit(C::bQEmpty + q_buf[0]);
             commit(C::bQEmpty + 2);
         };
-        // K_0 sits in the stage acquired in the previous tile's last block (or,
-        // for the first tile, in a stage of its own).
-        if (!warp_wait(bar(C::bQFull + q_buf[0]), (nq >> 1) & 1u, sc)) { alive = false; break; }
-        if (!have_k0 && !acquire(k0_stage)) { alive = false; break; }
-        have_k0 = false;
-        if (n0 > 0) issue_qk(0, k0_stage);
+        uint32_t ks, vs;
+        if (!warp_wait(bar(C::bQFull + q_buf[0]), (nq >> 1) & 1u, sc) || !acquire(ks)) { alive = false; break; }
+        if (n0 > 0) issue_qk(0, ks);
         issued = true;
         if (!warp_wait(bar(C::bQFull + 2), nq & 1u, sc)) { alive = false; break; }
         ptx::tc_fence_after_sync();
         ++nq;
-        if (n1 > 0) issue_qk(1, k0_stage);
-        commit(C::bKVEmpty + k0_stage);                // frees V_{n-1} of the previous tile and K_0
+        if (n1 > 0) issue_qk(1, ks);
+        commit(C::bKVEmpty + ks);
         if (n == 1) release_q();
         for (int j = 0; j < n; ++j) {
             const bool more = j + 1 < n;
-            uint32_t cur;                              // stage (V_j, K_{j+1})
-            if (!acquire(cur)) { alive = false; break; }
+            if (!acquire(vs)) { alive = false; break; }
             if (j < n0) {
                 if (!wait_p(0)) { alive = false; break; }
-                issue_pv(0, cur, j > 0);
+                issue_pv(0, vs, j > 0);
                 if (j == n0 - 1) commit(C::bOFull + 0);
-                if (j + 1 < n0) issue_qk(0, cur);
+            }
+            if (more) {
+                if (!acquire(ks)) { alive = false; break; }
+                if (j + 1 < n0) issue_qk(0, ks);
             }
             if (j < n1) {
                 if (!wait_p(1)) { alive = false; break; }
-                issue_pv(1, cur, j > 0);
+                issue_pv(1, vs, j > 0);
                 if (j == n1 - 1) commit(C::bOFull + 1);
             }
+            commit(C::bKVEmpty + vs);
             if (more) {
-                if (j + 1 < n1) issue_qk(1, cur);
+                if (j + 1 < n1) issue_qk(1, ks);
+                commit(C::bKVEmpty + ks);
                 if (j + 1 == n - 1) release_q();
-                commit(C::bKVEmpty + cur);
-            } else {
-                k0_stage = cur;                        // its K half is the next tile's K_0
-                have_k0 = true;
             }
         }
     }

@@ -34,11 +34,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// Raise the expected transaction bytes of the current phase without arriving.
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
 // True once the phase with the given parity has completed.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
@@ -70,19 +65,6 @@ __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, b
         : "r"((uint32_t)v), "r"(id), "r"(count)
         : "memory");
     return r != 0;
-}
-
-// Non-blocking test of a phase (no suspension): true once it has completed.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0;
 }
 
 // Make initialised barriers visible to the async proxy (TMA, tensor cores).
