@@ -329,13 +329,6 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         if (ok) ptx::tc_fence_after_sync();
         return ok;
     };
-    // V_j and K_{j+1} are not waited for here: the softmax warpgroup that hands
-    // over P_t(j) has already seen both land (mbarrier acquire), so "P_t(j)
-    // ready" also means they are in shared memory. Only the slot is tracked.
-    auto next_slot = [&](uint32_t& slot) {
-        slot = kv_use % C::kSlots;
-        ++kv_use;
-    };
     auto commit = [&](int b) {
         if (leader) ptx::tc_commit(bar(b));
     };
@@ -395,14 +388,14 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         if (n == 1) release_q();
         for (int j = 0; j < n; ++j) {
             const bool more = j + 1 < n;
-            next_slot(vs);
+            if (!acquire(vs)) { alive = false; break; }
             if (j < n0) {
                 if (!wait_p(0)) { alive = false; break; }
                 issue_pv(0, vs, j > 0);
                 if (j == n0 - 1) commit(C::bOFull + 0);
             }
             if (more) {
-                next_slot(ks);
+                if (!acquire(ks)) { alive = false; break; }
                 if (j + 1 < n0) issue_qk(0, ks);
             }
             if (j < n1) {
@@ -439,15 +432,12 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
     constexpr float kLn2 = 0.6931471805599453f;
     constexpr float kLog2e = 1.4426950408889634f;
     uint32_t s_phase = 0, o_phase = 0;
-    uint32_t kv_base = 0;            // K/V ring fills before the current tile (K_0, V_0, K_1, V_1, ...)
 
     for (int w = 0; w * (int)gridDim.x < p.n_tiles; ++w) {
         const int tile = tile_of_wave(w);
         if (tile >= p.n_tiles) continue;
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
         const int nb = ti.nb[wg];
-        const uint32_t fill0 = kv_base;
-        kv_base += 2u * (uint32_t)ti.n;
         const int row = ti.m0 + wg * kBlockM + r;
         const bool row_ok = row < p.Sq;
         uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (((size_t)ti.b * p.Sq + row) * p.Hq + ti.h) * D;
@@ -490,17 +480,6 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
             uint32_t sr[kBlockN];
 #pragma unroll
             for (int c = 0; c < kBlockN / 32; ++c) ptx::tmem_ld32(tS + 32 * c, sr + 32 * c);
-            // While S arrives: V_j (for P_t V_j) and, when this sub-tile has another
-            // block, K_{j+1} (for its next S) must have landed before P_t goes out.
-            bool kv_ok = true;
-            {
-                const uint32_t fv = fill0 + 2u * j + 1u;
-                kv_ok = wait_phase(bar(C::bKVFull + fv % C::kSlots), (fv / C::kSlots) & 1u, sc);
-                if (j + 1 < nb) {
-                    const uint32_t fk = fv + 1u;
-                    kv_ok = kv_ok && wait_phase(bar(C::bKVFull + fk % C::kSlots), (fk / C::kSlots) & 1u, sc);
-                }
-            }
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < kBlockN / 32; ++c) ptx::reg_fence32(sr + 32 * c);
@@ -601,8 +580,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
             ptx::tc_fence_before_sync();
             // All 128 rows of P_t are in TMEM once the warpgroup has met; one
             // thread then tells the MMA issuer (one arrival instead of 128).
-            ok = ptx::named_barrier_and(1 + wg, kBlockM, kv_ok);
-            if (!ok) break;
+            ptx::named_barrier_sync(1 + wg, kBlockM);
             if (r == 0) ptx::mbar_arrive(bar(C::bPFull + wg));
         }
         if (!ok) return;
