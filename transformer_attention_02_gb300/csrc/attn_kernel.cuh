@@ -91,21 +91,22 @@ struct TileCfg {
     static constexpr int kSlots = (D == 128) ? 4 : 8;         // K/V ring (K and V alternate)
     // Q sub-tile buffers: the lower sub-tile alternates between buffers 0 and 1
     // (so the next tile's is loaded a whole tile ahead), the upper uses buffer 2.
-    static constexpr int kQBufs = 3;
+    static constexpr int kQ1Bufs = 1;                         // buffers of the upper sub-tile
+    static constexpr int kQBufs = 2 + kQ1Bufs;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = kQBufs * kTileBytes;
     static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
     // barrier indices
-    static constexpr int bQFull = 0;        // [kQBufs]
-    static constexpr int bQEmpty = 3;       // [kQBufs]
-    static constexpr int bSFull = 6;        // [2]
-    static constexpr int bPFull = 8;        // [2]
-    static constexpr int bOFull = 10;       // [2]
-    static constexpr int bDrain = 12;
-    static constexpr int bStall = 13;
-    static constexpr int bKVFull = 14;      // [kSlots]
-    static constexpr int bKVEmpty = 14 + kSlots;
-    static constexpr int kNumBars = 14 + 2 * kSlots;
+    static constexpr int bQFull = 0;                  // [kQBufs]
+    static constexpr int bQEmpty = kQBufs;            // [kQBufs]
+    static constexpr int bSFull = 2 * kQBufs;         // [2]
+    static constexpr int bPFull = bSFull + 2;         // [2]
+    static constexpr int bOFull = bPFull + 2;         // [2]
+    static constexpr int bDrain = bOFull + 2;
+    static constexpr int bStall = bDrain + 1;
+    static constexpr int bKVFull = bStall + 1;        // [kSlots]
+    static constexpr int bKVEmpty = bKVFull + kSlots;
+    static constexpr int kNumBars = bKVEmpty + kSlots;
     static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemUsed = kAbortOff + 4;
@@ -264,7 +265,7 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
     const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
-    uint32_t uses[C::kQBufs] = {0, 0, 0};       // loads issued into each buffer
+    uint32_t uses[C::kQBufs] = {};              // loads issued into each buffer
     uint32_t nq = 0;                            // work tiles with at least one block
     auto load = [&](int buf, int row0, const TileInfo& ti) -> bool {
         if (uses[buf] > 0 && !warp_wait(bar(C::bQEmpty + buf), (uses[buf] - 1) & 1u, sc)) return false;
@@ -282,7 +283,7 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
         if (tile >= p.n_tiles) continue;
         const TileInfo ti = tile_info<CAUSAL>(tile, p);
         if (ti.n == 0) continue;
-        if (!load(nq & 1, ti.m0, ti) || !load(2, ti.m0 + kBlockM, ti)) break;
+        if (!load(nq & 1, ti.m0, ti) || !load(2 + nq % C::kQ1Bufs, ti.m0 + kBlockM, ti)) break;
         ++nq;
     }
     // Shut down: wait until every copy this warp started has landed.
@@ -372,15 +373,16 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         // use), upper sub-tile in buffer 2 (its nq-th use). Both phases are consumed
         // even when a sub-tile has no block, to keep the parities in step.
         q_buf[0] = nq & 1u;
+        q_buf[1] = 2 + nq % C::kQ1Bufs;
         auto release_q = [&]() {
             commit(C::bQEmpty + q_buf[0]);
-            commit(C::bQEmpty + 2);
+            commit(C::bQEmpty + q_buf[1]);
         };
         uint32_t ks, vs;
         if (!warp_wait(bar(C::bQFull + q_buf[0]), (nq >> 1) & 1u, sc) || !acquire(ks)) { alive = false; break; }
         if (n0 > 0) issue_qk(0, ks);
         issued = true;
-        if (!warp_wait(bar(C::bQFull + 2), nq & 1u, sc)) { alive = false; break; }
+        if (!warp_wait(bar(C::bQFull + q_buf[1]), (nq / C::kQ1Bufs) & 1u, sc)) { alive = false; break; }
         ptx::tc_fence_after_sync();
         ++nq;
         if (n1 > 0) issue_qk(1, ks);
