@@ -47,11 +47,11 @@ class Oracle:
             build(output=library)
         self.path = library
         self._lib = ctypes.CDLL(library)
-        f = self._lib.oracle_attn_fwd
         P = ctypes.c_void_p
         I = ctypes.c_int
+        f = self._lib.oracle_attn_fwd_rope
         f.argtypes = [P, P, P, I, P, I, I, I, I, I, I, I, ctypes.c_double,
-                      I, P, P, I, I, P, P, P, I]
+                      I, P, P, I, I, P, P, P, I, ctypes.c_double, ctypes.c_longlong, ctypes.c_longlong]
         f.restype = I
         self._lib.oracle_num_threads.restype = I
 
@@ -60,13 +60,16 @@ class Oracle:
 
     def attention(self, q, k, v, *, mask_kind: int, mask=None, scale=None,
                   dtype: str = "bf16", slices=None, rows=None, n_threads: int = 0,
-                  want_psum: bool = False):
+                  want_psum: bool = False, rope_base: float = 0.0, q_pos0: int = 0, k_pos0: int = 0):
         """FP64 attention on 16-bit inputs.
 
         q: (B,Sq,Hq,D), k/v: (B,Sk,Hkv,D) as uint16/int16 bit patterns (numpy)
         of bf16 or fp16 values; mask: (B,Sq,Sk) float32 for the additive kinds.
         slices: list of (b, h) pairs (default: every slice in (b, h) order);
         rows: (begin, end) query-row range (default: all rows).
+        rope_base > 0 rotates q and k (rotary position embedding, interleaved
+        pairs, angle pos * rope_base^(-2i/D)) with query row i at position
+        q_pos0 + i and key j at k_pos0 + j.
 
         Returns (o, lse[, psum]) with o of shape (n_slices, rows, D) and lse of
         shape (n_slices, rows), both float64. With the default slices and rows,
@@ -94,13 +97,14 @@ class Oracle:
         lse = np.zeros((n, r1 - r0), dtype=np.float64)
         psum = np.zeros((n, r1 - r0), dtype=np.float64) if want_psum else None
         sc = float("nan") if scale is None else float(scale)
-        rc = self._lib.oracle_attn_fwd(
+        rc = self._lib.oracle_attn_fwd_rope(
             q.ctypes.data, k.ctypes.data, v.ctypes.data, DTYPES[dtype],
             mask.ctypes.data if additive else None, int(mask_kind),
             B, Hq, Hkv, Sq, Sk, D, sc,
             n, sb.ctypes.data, sh.ctypes.data, r0, r1,
             o.ctypes.data, lse.ctypes.data,
-            psum.ctypes.data if want_psum else None, int(n_threads))
+            psum.ctypes.data if want_psum else None, int(n_threads),
+            float(rope_base), int(q_pos0), int(k_pos0))
         if rc != 0:
             raise ValueError(f"oracle rejected its arguments (rc={rc})")
         return (o, lse, psum) if want_psum else (o, lse)

@@ -37,6 +37,16 @@
  *
  * Inputs are the raw 16-bit patterns of bf16 (dtype 0) or IEEE fp16 (dtype 1)
  * values; each is widened to double exactly.
+ *
+ * Optional rotary position embedding (oracle_attn_fwd_rope), applied to q and
+ * k before the scores ("ATB engineering guide" §4.1 pattern 5, RoPE fused with
+ * attention; §8.4, interleaved pairs with rotary base 10000): the pair
+ * (x[2i], x[2i+1]) of a head vector at position pos turns by the angle
+ * pos * base^(-2i/D):
+ *   (x[2i], x[2i+1]) -> (x[2i] cos - x[2i+1] sin, x[2i+1] cos + x[2i] sin).
+ * Query row i sits at position q_pos0 + i, key j at k_pos0 + j. (The page's
+ * listing doubles the exponent and spans the whole hidden size; the per-head
+ * form above is the reading taken.)
  */
 #include <math.h>
 #include <stdint.h>
@@ -77,6 +87,17 @@ static double widen(uint16_t bits, int dtype) {
     return dtype == ORACLE_DTYPE_F16 ? widen_f16(bits) : widen_bf16(bits);
 }
 
+/* Rotary position embedding of one head vector, in place. */
+static void rope_rotate(double *x, int D, long long pos, double base) {
+    for (int i = 0; i < D / 2; ++i) {
+        const double theta = (double)pos * pow(base, -2.0 * i / D);
+        const double c = cos(theta), s = sin(theta);
+        const double x0 = x[2 * i], x1 = x[2 * i + 1];
+        x[2 * i] = x0 * c - x1 * s;
+        x[2 * i + 1] = x1 * c + x0 * s;
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
@@ -98,12 +119,16 @@ int oracle_num_threads(void) {
  *
  * Returns 0 on success, -1 on an invalid argument.
  */
-int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
-                    const float *mask, int mask_kind,
-                    int B, int Hq, int Hkv, int Sq, int Sk, int D, double scale,
-                    int n_slices, const int32_t *slice_b, const int32_t *slice_h,
-                    int row_begin, int row_end,
-                    double *o, double *lse, double *psum, int n_threads) {
+/* As oracle_attn_fwd, with q and k rotated (rope_base > 0) or not (rope_base = 0). */
+int oracle_attn_fwd_rope(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                         const float *mask, int mask_kind,
+                         int B, int Hq, int Hkv, int Sq, int Sk, int D, double scale,
+                         int n_slices, const int32_t *slice_b, const int32_t *slice_h,
+                         int row_begin, int row_end,
+                         double *o, double *lse, double *psum, int n_threads,
+                         double rope_base, long long q_pos0, long long k_pos0) {
+    if (rope_base < 0.0 || (rope_base > 0.0 && (D % 2 != 0))) return -1;
+    const int rope = rope_base > 0.0;
     if (!q || !k || !v || !o || !lse || !slice_b || !slice_h) return -1;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return -1;
     if (Hq % Hkv != 0) return -1;
@@ -139,6 +164,8 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
                 kd[j * D + d] = widen(k[src], dtype);
                 vd[j * D + d] = widen(v[src], dtype);
             }
+        if (rope)
+            for (long long j = 0; j < Sk; ++j) rope_rotate(kd + j * D, D, k_pos0 + j, rope_base);
 
         int failed = 0;
 #pragma omp parallel
@@ -155,6 +182,7 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
                     double *orow = o + ((size_t)s * rows + r) * D;
                     for (int d = 0; d < D; ++d)
                         qd[d] = widen(q[(((size_t)b * Sq + i) * Hq + h) * D + d], dtype);
+                    if (rope) rope_rotate(qd, D, q_pos0 + i, rope_base);
 
                     /* Scores, then pass 1: the row maximum. */
                     double m = -INFINITY;
@@ -202,4 +230,15 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
         if (failed) return -1;
     }
     return 0;
+}
+
+int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
+                    const float *mask, int mask_kind,
+                    int B, int Hq, int Hkv, int Sq, int Sk, int D, double scale,
+                    int n_slices, const int32_t *slice_b, const int32_t *slice_h,
+                    int row_begin, int row_end,
+                    double *o, double *lse, double *psum, int n_threads) {
+    return oracle_attn_fwd_rope(q, k, v, dtype, mask, mask_kind, B, Hq, Hkv, Sq, Sk, D, scale,
+                                n_slices, slice_b, slice_h, row_begin, row_end, o, lse, psum, n_threads,
+                                0.0, 0, 0);
 }

@@ -352,9 +352,80 @@ def pin_subset_matches_full(orc):
         assert np.array_equal(ls[n], lf[b * Hq + h, 5:17])
 
 
+def _rope_py(t, pos0, base):
+    """Rotate a (B, S, H, D) tensor in pure Python: pair (2i, 2i+1) of the vector
+    at sequence index s turns by (pos0 + s) * base ** (-2 i / D)."""
+    x = t.double().tolist()
+    B, S, H, D = t.shape
+    for b in range(B):
+        for si in range(S):
+            ang0 = pos0 + si
+            for h in range(H):
+                v = x[b][si][h]
+                for i in range(D // 2):
+                    th = ang0 * base ** (-2.0 * i / D)
+                    c, sn = math.cos(th), math.sin(th)
+                    a, bb = v[2 * i], v[2 * i + 1]
+                    v[2 * i], v[2 * i + 1] = a * c - bb * sn, bb * c + a * sn
+    return torch.tensor(x, dtype=torch.float64)
+
+
+def pin_rope_brute_force(orc):
+    """With rotary embedding: oracle == rotate (pure Python) then brute-force attention."""
+    for n, (B, Hq, Hkv, Sq, Sk, D, kind, qp, kp) in enumerate([
+            (1, 2, 2, 5, 7, 8, NONE, 0, 0),
+            (2, 4, 2, 4, 9, 8, CAUSAL, 5, 0),
+            (1, 2, 1, 6, 6, 4, CAUSAL_ADDITIVE, 3, 3)]):
+        q = _rand16((B, Sq, Hq, D), 1200 + n)
+        k = _rand16((B, Sk, Hkv, D), 1210 + n)
+        v = _rand16((B, Sk, Hkv, D), 1220 + n)
+        mask = _finite_mask(B, Sq, Sk, 1230 + n, n_neg_inf=1) if kind >= ADDITIVE else None
+        o, lse = _run(orc, q, k, v, kind, mask, rope_base=10000.0, q_pos0=qp, k_pos0=kp)
+        ob, lb = _brute(_rope_py(q, qp, 10000.0), _rope_py(k, kp, 10000.0), v, kind, mask, 1.0 / math.sqrt(D))
+        _close(o, ob, tol=1e-11, what=f"rope brute {n} O")
+        _close(lse, lb, tol=1e-11, what=f"rope brute {n} LSE")
+
+
+def pin_rope_two_dim_closed_form(orc):
+    """D = 2 (one pair, frequency 1): q = (1, 0) at position p, k = (1, 0) at position p'
+    gives the single logit scale * cos(p' - p), so lse = scale * cos(p' - p)."""
+    q = torch.tensor([1.0, 0.0]).reshape(1, 1, 1, 2).to(torch.bfloat16)
+    k = torch.tensor([1.0, 0.0]).reshape(1, 1, 1, 2).to(torch.bfloat16)
+    v = torch.tensor([0.5, -2.0]).reshape(1, 1, 1, 2).to(torch.bfloat16)
+    for qp, kp in ((3, 10), (10, 3), (0, 0)):
+        o, lse = _run(orc, q, k, v, NONE, scale=0.5, rope_base=10000.0, q_pos0=qp, k_pos0=kp)
+        assert abs(lse[0, 0] - 0.5 * math.cos(kp - qp)) <= 1e-14
+        assert np.array_equal(o[0, 0], [0.5, -2.0])
+
+
+def pin_rope_depends_on_relative_position(orc):
+    """Shifting every query and key position by the same amount changes nothing."""
+    B, Hq, Sq, Sk, D = 1, 2, 6, 9, 16
+    q = _rand16((B, Sq, Hq, D), 1301)
+    k = _rand16((B, Sk, Hq, D), 1302)
+    v = _rand16((B, Sk, Hq, D), 1303)
+    o0, l0 = _run(orc, q, k, v, CAUSAL, rope_base=10000.0, q_pos0=3, k_pos0=0)
+    o1, l1 = _run(orc, q, k, v, CAUSAL, rope_base=10000.0, q_pos0=40, k_pos0=37)
+    _close(o1, o0, tol=1e-10, what="rope shift O")
+    _close(l1, l0, tol=1e-10, what="rope shift LSE")
+    o2, _ = _run(orc, q, k, v, CAUSAL, rope_base=10000.0, q_pos0=4, k_pos0=0)
+    assert not np.allclose(o2, o0, atol=1e-6)          # a different offset does change it
+
+
+def pin_rope_position_zero_is_identity(orc):
+    """A single query and key both at position 0: the rotation is the identity."""
+    q = _rand16((1, 1, 2, 16), 1401)
+    k = _rand16((1, 1, 2, 16), 1402)
+    v = _rand16((1, 1, 2, 16), 1403)
+    assert all(np.array_equal(a, b) for a, b in zip(_run(orc, q, k, v, NONE, rope_base=10000.0),
+                                                    _run(orc, q, k, v, NONE)))
+
+
 ALL_PINS = [
     pin_brute_force, pin_brute_force_f16, pin_widening_exact, pin_sdpa_float64,
     pin_rowsum_one, pin_constant_v, pin_zero_q, pin_causal_row0, pin_shift_invariance,
     pin_key_permutation, pin_gqa_equals_mha, pin_scale_half, pin_default_scale,
     pin_two_key_closed_form, pin_fully_masked_row, pin_subset_matches_full,
+    pin_rope_brute_force, pin_rope_two_dim_closed_form, pin_rope_depends_on_relative_position,
+    pin_rope_position_zero_is_identity,
 ]

@@ -30,6 +30,9 @@ MUTATIONS = {
     "bf16_shift": ("uint32_t u = (uint32_t)bits << 16;", "uint32_t u = (uint32_t)bits << 15;"),
     "f16_bias": ("expo - 25);", "expo - 24);"),
     "default_scale_sqrt_missing": ("scale = 1.0 / sqrt((double)D);", "scale = 1.0 / (double)D;"),
+    "rope_rotation_sign": ("x[2 * i] = x0 * c - x1 * s;", "x[2 * i] = x0 * c + x1 * s;"),
+    "rope_frequency_exponent": ("pow(base, -2.0 * i / D)", "pow(base, -1.0 * i / D)"),
+    "rope_query_position": ("rope_rotate(qd, D, q_pos0 + i, rope_base);", "rope_rotate(qd, D, k_pos0 + i, rope_base);"),
 }
 
 
