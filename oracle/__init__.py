@@ -43,7 +43,9 @@ class Oracle:
     """ctypes view of one compiled oracle library."""
 
     def __init__(self, library: str = LIBRARY):
-        if not os.path.exists(library):
+        stale = library == LIBRARY and os.path.exists(library) and \
+            os.path.getmtime(library) < os.path.getmtime(SOURCE)
+        if not os.path.exists(library) or stale:
             build(output=library)
         self.path = library
         self._lib = ctypes.CDLL(library)
@@ -51,7 +53,7 @@ class Oracle:
         I = ctypes.c_int
         f = self._lib.oracle_attn_fwd_rope
         f.argtypes = [P, P, P, I, P, I, I, I, I, I, I, I, ctypes.c_double,
-                      I, P, P, I, I, P, P, P, I, ctypes.c_double, ctypes.c_longlong, ctypes.c_longlong]
+                      I, P, P, I, I, P, P, P, I, ctypes.c_double, ctypes.c_longlong, ctypes.c_longlong, I]
         f.restype = I
         self._lib.oracle_num_threads.restype = I
 
@@ -60,7 +62,8 @@ class Oracle:
 
     def attention(self, q, k, v, *, mask_kind: int, mask=None, scale=None,
                   dtype: str = "bf16", slices=None, rows=None, n_threads: int = 0,
-                  want_psum: bool = False, rope_base: float = 0.0, q_pos0: int = 0, k_pos0: int = 0):
+                  want_psum: bool = False, rope_base: float = 0.0, q_pos0: int = 0, k_pos0: int = 0,
+                  rope_round: bool = False):
         """FP64 attention on 16-bit inputs.
 
         q: (B,Sq,Hq,D), k/v: (B,Sk,Hkv,D) as uint16/int16 bit patterns (numpy)
@@ -69,7 +72,9 @@ class Oracle:
         rows: (begin, end) query-row range (default: all rows).
         rope_base > 0 rotates q and k (rotary position embedding, interleaved
         pairs, angle pos * rope_base^(-2i/D)) with query row i at position
-        q_pos0 + i and key j at k_pos0 + j.
+        q_pos0 + i and key j at k_pos0 + j; rope_round rounds each rotated
+        element to the nearest value of `dtype` (ties to even), the reading in
+        which the rotated q and k are held in the input's 16-bit type.
 
         Returns (o, lse[, psum]) with o of shape (n_slices, rows, D) and lse of
         shape (n_slices, rows), both float64. With the default slices and rows,
@@ -104,7 +109,7 @@ class Oracle:
             n, sb.ctypes.data, sh.ctypes.data, r0, r1,
             o.ctypes.data, lse.ctypes.data,
             psum.ctypes.data if want_psum else None, int(n_threads),
-            float(rope_base), int(q_pos0), int(k_pos0))
+            float(rope_base), int(q_pos0), int(k_pos0), int(bool(rope_round)))
         if rc != 0:
             raise ValueError(f"oracle rejected its arguments (rc={rc})")
         return (o, lse, psum) if want_psum else (o, lse)

@@ -46,7 +46,10 @@
  *   (x[2i], x[2i+1]) -> (x[2i] cos - x[2i+1] sin, x[2i+1] cos + x[2i] sin).
  * Query row i sits at position q_pos0 + i, key j at k_pos0 + j. (The page's
  * listing doubles the exponent and spans the whole hidden size; the per-head
- * form above is the reading taken.)
+ * form above is the reading taken.) With rope_round set, each rotated element
+ * is then rounded to the nearest value of the input's 16-bit type (ties to
+ * even), as §8.4's reference rotation hands back its result in the input's
+ * half-precision type; without it the rotated vectors stay exact.
  */
 #include <math.h>
 #include <stdint.h>
@@ -87,14 +90,36 @@ static double widen(uint16_t bits, int dtype) {
     return dtype == ORACLE_DTYPE_F16 ? widen_f16(bits) : widen_bf16(bits);
 }
 
+/* Nearest value of the 16-bit type (ties to even), as a double: bf16 keeps 8
+ * significant bits and the binary32 exponent range (smallest normal 2^-126),
+ * fp16 keeps 11 (smallest normal 2^-14); both underflow gradually and go to
+ * infinity past their largest finite value. */
+static double narrow(double x, int dtype) {
+    if (x == 0.0 || !isfinite(x)) return x;
+    const int bits = dtype == ORACLE_DTYPE_F16 ? 11 : 8;
+    const int emin = dtype == ORACLE_DTYPE_F16 ? -14 : -126;
+    const double maxf = dtype == ORACLE_DTYPE_F16 ? 65504.0 : ldexp(255.0, 120);
+    int e;
+    frexp(x, &e);                          /* |x| in [2^(e-1), 2^e) */
+    int lead = e - 1;
+    if (lead < emin) lead = emin;
+    const double ulp = ldexp(1.0, lead - (bits - 1));
+    const double r = nearbyint(x / ulp) * ulp;     /* x / ulp is exact; default rounding is to even */
+    return fabs(r) > maxf ? copysign(INFINITY, x) : r;
+}
+
 /* Rotary position embedding of one head vector, in place. */
-static void rope_rotate(double *x, int D, long long pos, double base) {
+static void rope_rotate(double *x, int D, long long pos, double base, int round_to, int dtype) {
     for (int i = 0; i < D / 2; ++i) {
         const double theta = (double)pos * pow(base, -2.0 * i / D);
         const double c = cos(theta), s = sin(theta);
         const double x0 = x[2 * i], x1 = x[2 * i + 1];
         x[2 * i] = x0 * c - x1 * s;
         x[2 * i + 1] = x1 * c + x0 * s;
+        if (round_to) {
+            x[2 * i] = narrow(x[2 * i], dtype);
+            x[2 * i + 1] = narrow(x[2 * i + 1], dtype);
+        }
     }
 }
 
@@ -126,7 +151,7 @@ int oracle_attn_fwd_rope(const uint16_t *q, const uint16_t *k, const uint16_t *v
                          int n_slices, const int32_t *slice_b, const int32_t *slice_h,
                          int row_begin, int row_end,
                          double *o, double *lse, double *psum, int n_threads,
-                         double rope_base, long long q_pos0, long long k_pos0) {
+                         double rope_base, long long q_pos0, long long k_pos0, int rope_round) {
     if (rope_base < 0.0 || (rope_base > 0.0 && (D % 2 != 0))) return -1;
     const int rope = rope_base > 0.0;
     if (!q || !k || !v || !o || !lse || !slice_b || !slice_h) return -1;
@@ -165,7 +190,7 @@ int oracle_attn_fwd_rope(const uint16_t *q, const uint16_t *k, const uint16_t *v
                 vd[j * D + d] = widen(v[src], dtype);
             }
         if (rope)
-            for (long long j = 0; j < Sk; ++j) rope_rotate(kd + j * D, D, k_pos0 + j, rope_base);
+            for (long long j = 0; j < Sk; ++j) rope_rotate(kd + j * D, D, k_pos0 + j, rope_base, rope_round, dtype);
 
         int failed = 0;
 #pragma omp parallel
@@ -182,7 +207,7 @@ int oracle_attn_fwd_rope(const uint16_t *q, const uint16_t *k, const uint16_t *v
                     double *orow = o + ((size_t)s * rows + r) * D;
                     for (int d = 0; d < D; ++d)
                         qd[d] = widen(q[(((size_t)b * Sq + i) * Hq + h) * D + d], dtype);
-                    if (rope) rope_rotate(qd, D, q_pos0 + i, rope_base);
+                    if (rope) rope_rotate(qd, D, q_pos0 + i, rope_base, rope_round, dtype);
 
                     /* Scores, then pass 1: the row maximum. */
                     double m = -INFINITY;
@@ -240,5 +265,5 @@ int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int
                     double *o, double *lse, double *psum, int n_threads) {
     return oracle_attn_fwd_rope(q, k, v, dtype, mask, mask_kind, B, Hq, Hkv, Sq, Sk, D, scale,
                                 n_slices, slice_b, slice_h, row_begin, row_end, o, lse, psum, n_threads,
-                                0.0, 0, 0);
+                                0.0, 0, 0, 0);
 }

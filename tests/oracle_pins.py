@@ -421,11 +421,50 @@ def pin_rope_position_zero_is_identity(orc):
                                                     _run(orc, q, k, v, NONE)))
 
 
+def _held_in(t64, dtype):
+    """Round a float64 tensor to the 16-bit type with PyTorch's own conversion."""
+    return t64.to(torch.bfloat16 if dtype == "bf16" else torch.float16).double()
+
+
+def pin_rope_round_brute_force(orc):
+    """rope_round: oracle == rotate (pure Python), round with PyTorch's 16-bit
+    conversion, then brute-force attention; bf16 and fp16."""
+    for n, (B, Hq, Hkv, Sq, Sk, D, kind, qp, kp, dt) in enumerate([
+            (1, 2, 2, 5, 7, 8, NONE, 0, 0, "bf16"),
+            (2, 4, 2, 4, 9, 8, CAUSAL, 5, 2, "bf16"),
+            (1, 2, 1, 6, 6, 4, CAUSAL, 30, 27, "f16")]):
+        tdt = torch.bfloat16 if dt == "bf16" else torch.float16
+        q = _rand16((B, Sq, Hq, D), 1500 + n, dtype=tdt)
+        k = _rand16((B, Sk, Hkv, D), 1510 + n, dtype=tdt)
+        v = _rand16((B, Sk, Hkv, D), 1520 + n, dtype=tdt)
+        o, lse = _run(orc, q, k, v, kind, None, dtype=dt, rope_base=10000.0, q_pos0=qp, k_pos0=kp,
+                      rope_round=True)
+        ob, lb = _brute(_held_in(_rope_py(q, qp, 10000.0), dt), _held_in(_rope_py(k, kp, 10000.0), dt), v,
+                        kind, None, 1.0 / math.sqrt(D))
+        _close(o, ob, tol=1e-11, what=f"rope round brute {n} O")
+        _close(lse, lb, tol=1e-11, what=f"rope round brute {n} LSE")
+
+
+def pin_rope_round_single_key_closed_form(orc):
+    """D = 2, one key (1, 0) at position 0 (no rotation) and the query (1, 0) at
+    position p: the only logit is scale * q_rot[0], and q_rot[0] is cos(p) held
+    in the 16-bit type, so lse = scale * round16(cos p) and o = v."""
+    for dt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        one = torch.tensor([1.0, 0.0]).reshape(1, 1, 1, 2).to(tdt)
+        v = torch.tensor([0.25, -3.0]).reshape(1, 1, 1, 2).to(tdt)
+        for p in (1, 2, 5, 7, 11, 20, 33, 100):
+            o, lse = _run(orc, one, one, v, NONE, scale=1.0, dtype=dt, rope_base=10000.0, q_pos0=p,
+                          k_pos0=0, rope_round=True)
+            want = float(torch.tensor(math.cos(p), dtype=torch.float64).to(tdt).double())
+            assert lse[0, 0] == want, (dt, p, lse[0, 0], want)
+            assert np.array_equal(o[0, 0], [0.25, -3.0])
+
+
 ALL_PINS = [
     pin_brute_force, pin_brute_force_f16, pin_widening_exact, pin_sdpa_float64,
     pin_rowsum_one, pin_constant_v, pin_zero_q, pin_causal_row0, pin_shift_invariance,
     pin_key_permutation, pin_gqa_equals_mha, pin_scale_half, pin_default_scale,
     pin_two_key_closed_form, pin_fully_masked_row, pin_subset_matches_full,
     pin_rope_brute_force, pin_rope_two_dim_closed_form, pin_rope_depends_on_relative_position,
-    pin_rope_position_zero_is_identity,
+    pin_rope_position_zero_is_identity, pin_rope_round_brute_force, pin_rope_round_single_key_closed_form,
 ]

@@ -32,7 +32,13 @@ MUTATIONS = {
     "default_scale_sqrt_missing": ("scale = 1.0 / sqrt((double)D);", "scale = 1.0 / (double)D;"),
     "rope_rotation_sign": ("x[2 * i] = x0 * c - x1 * s;", "x[2 * i] = x0 * c + x1 * s;"),
     "rope_frequency_exponent": ("pow(base, -2.0 * i / D)", "pow(base, -1.0 * i / D)"),
-    "rope_query_position": ("rope_rotate(qd, D, q_pos0 + i, rope_base);", "rope_rotate(qd, D, k_pos0 + i, rope_base);"),
+    "rope_query_position": ("rope_rotate(qd, D, q_pos0 + i, rope_base, rope_round, dtype);",
+                            "rope_rotate(qd, D, k_pos0 + i, rope_base, rope_round, dtype);"),
+    "rope_round_truncates": ("nearbyint(x / ulp) * ulp", "trunc(x / ulp) * ulp"),
+    "rope_round_types_swapped": ("const int bits = dtype == ORACLE_DTYPE_F16 ? 11 : 8;",
+                                 "const int bits = dtype == ORACLE_DTYPE_F16 ? 8 : 11;"),
+    "rope_round_skips_keys": ("rope_rotate(kd + j * D, D, k_pos0 + j, rope_base, rope_round, dtype);",
+                              "rope_rotate(kd + j * D, D, k_pos0 + j, rope_base, 0, dtype);"),
 }
 
 
