@@ -14,6 +14,10 @@ inputs resident in device memory. Prints ONE JSON line on rank 0.
   roofline   the kernel against the measured dense bf16 tensor peak
   cpu_baseline  the FP64 oracle on this host's cores, on a bounded sample
 
+`--rope` runs the same workload with the rotary position embedding: each step
+rotates the keys once (bandwidth-bound pass) and runs the attention kernel that
+rotates the queries at tile load; `value` covers both launches, `roofline` the
+attention kernel alone, and the FLOP count stays the attention's.
 `--impl reference` times the oracle (the only reference implementation this
 method has) on the same workload and metric instead.
 Multi-GPU (torchrun): every rank runs its own replica of the workload on its
@@ -46,9 +50,10 @@ METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense bf16 tensor pe
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ["transformer_attention_02_gb300/csrc/attn_kernel.cuh",
-                  "transformer_attention_02_gb300/csrc/ptx.cuh",
-                  "transformer_attention_02_gb300/csrc/attn_api.cu"]
+KERNEL_SOURCES = ["transformer_attention_02_gb300/csrc/" + f for f in (
+    "attn_kernel.cuh", "ptx.cuh", "attn_api.cu", "attn_launch.h", "attn_fwd_inst.cuh", "fwd_bf16.cu",
+    "fwd_f16.cu", "fwd_rope_bf16.cu", "fwd_rope_f16.cu")]
+ROPE_BASE = 10000.0
 
 
 # ------------------------------------------------------------------ helpers
@@ -182,7 +187,7 @@ def row_flops(cfg: I.AttnConfig, r0: int, r1: int) -> float:
     return tot
 
 
-def oracle_sample(cfg, q, k, v, mask, target_s: float, slices_cycle):
+def oracle_sample(cfg, q, k, v, mask, target_s: float, slices_cycle, rope_kw=None):
     """Time the oracle on whole (b, h) slices until about target_s seconds of
     work are done (at least one slice). Returns (seconds, flops, n_slices, threads)."""
     import oracle
@@ -193,7 +198,8 @@ def oracle_sample(cfg, q, k, v, mask, target_s: float, slices_cycle):
     done, spent, n = 0.0, 0.0, 0
     while n == 0 or (spent < target_s and n < len(slices_cycle)):
         t0 = time.perf_counter()
-        orc.attention(qb, kb, vb, mask_kind=cfg.mask_kind, mask=mk, slices=[slices_cycle[n]])
+        orc.attention(qb, kb, vb, mask_kind=cfg.mask_kind, mask=mk, slices=[slices_cycle[n]],
+                      **(rope_kw or {}))
         spent += time.perf_counter() - t0
         done += per_slice
         n += 1
@@ -223,17 +229,19 @@ def run_reference(args, cfg):
     qb, kb, vb = I.bits(q), I.bits(k), I.bits(v)
     mk = None if mask is None else mask.numpy()
     slices = spread_slices(cfg)
+    rope_kw = dict(rope_base=ROPE_BASE, rope_round=True) if args.rope else {}
     # size each step (a window of query rows of one slice) so the whole run takes about a minute
     budget = 60.0 / max(1, args.steps + args.warmup)
     t0 = time.perf_counter()
-    orc.attention(qb, kb, vb, mask_kind=cfg.mask_kind, mask=mk, slices=[slices[0]], rows=(0, 16))
+    orc.attention(qb, kb, vb, mask_kind=cfg.mask_kind, mask=mk, slices=[slices[0]], rows=(0, 16), **rope_kw)
     per_row = max(1e-6, (time.perf_counter() - t0) / 16)
     rows = int(max(8, min(cfg.Sq, budget / per_row / 1.5)))
 
     def step(i):
         b, h = slices[i % len(slices)]
         r0 = (i * 977 * rows) % max(1, cfg.Sq - rows + 1)
-        orc.attention(qb, kb, vb, mask_kind=cfg.mask_kind, mask=mk, slices=[(b, h)], rows=(r0, r0 + rows))
+        orc.attention(qb, kb, vb, mask_kind=cfg.mask_kind, mask=mk, slices=[(b, h)], rows=(r0, r0 + rows),
+                      **rope_kw)
         return row_flops(cfg, r0, r0 + rows)
 
     for i in range(args.warmup):
@@ -248,7 +256,7 @@ def run_reference(args, cfg):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": config_json(cfg),
+        "data": "synthetic", "config": config_json(cfg, args.rope),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
                          "sample": f"{args.steps} steps of {rows} query rows of one (b,h) slice each, "
                                    f"slices spread over the batch and heads"},
@@ -260,8 +268,10 @@ def run_reference(args, cfg):
 
 # ---------------------------------------------------------------- GPU arm
 
-def config_json(cfg):
-    return {"workload": cfg.name, "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "Sq": cfg.Sq, "Sk": cfg.Sk,
+def config_json(cfg, rope=False):
+    extra = {"rope": {"base": ROPE_BASE, "q_pos0": 0, "k_pos0": 0, "pairs": "interleaved"}} if rope else {}
+    return {**extra, "workload": cfg.name + ("+rope" if rope else ""), "B": cfg.B, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
+            "Sq": cfg.Sq, "Sk": cfg.Sk,
             "D": cfg.D, "mask": ("causal" if cfg.causal else "none") + ("+additive" if cfg.additive_mask else ""),
             "values": cfg.values, "seed": cfg.seed,
             "l2": "flushed before every timed step (untimed 256 MiB write); device time = CUDA events "
@@ -288,8 +298,24 @@ def run_ours(args, cfg):
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    if args.rope:
+        table = A.rope_table(max(cfg.Sq, cfg.Sk), cfg.D, ROPE_BASE, stream=stream)
+        k_rot = torch.empty_like(kd)
+
+    def launch_keys():          # rotary variant only: rotate each key once
+        A.rope_apply(kd, table, pos0=0, out=k_rot, stream=stream)
+
+    def launch_attention():
+        if args.rope:
+            A.attention_rope(qd, k_rot, vd, table, k_rot=None, causal=cfg.causal, mask=md, out=o, lse=lse,
+                             stream=stream)
+        else:
+            A.attention(qd, kd, vd, causal=cfg.causal, mask=md, out=o, lse=lse, stream=stream)
+
     def launch():
-        A.attention(qd, kd, vd, causal=cfg.causal, mask=md, out=o, lse=lse, stream=stream)
+        if args.rope:
+            launch_keys()
+        launch_attention()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -303,6 +329,7 @@ def run_ours(args, cfg):
         clocks.start()
         time.sleep(0.3)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize(dev)
@@ -310,13 +337,18 @@ def run_ours(args, cfg):
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        launch()
+        if args.rope:
+            launch_keys()
+        mids[i].record(stream)
+        launch_attention()
         ends[i].record(stream)
     torch.cuda.synchronize(dev)
     barrier()
     t_wall1 = time.time()
-    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    local_s = sum(kernel_ms) / 1e3
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kernel_ms = [m.elapsed_time(e) for m, e in zip(mids, ends)]      # the attention kernel alone
+    key_ms = [s.elapsed_time(m) for s, m in zip(starts, mids)] if args.rope else None
+    local_s = sum(step_ms) / 1e3
     max_s = reduce_max(local_s, dev)
     if A.attn_last_status(stream.cuda_stream) != A.ATTN_OK:
         raise RuntimeError("kernel reported a device timeout in the timed region")
@@ -365,14 +397,14 @@ def run_ours(args, cfg):
     value = whole_job_tflops(flops, args.steps, world, max_s)
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    per_launch_s = local_s / args.steps
+    per_launch_s = sum(kernel_ms) / 1e3 / args.steps
     achieved = flops / per_launch_s / 1e12
-    traffic = profiled_traffic(cfg.name)
+    traffic = profiled_traffic(cfg.name + ("_rope" if args.rope else ""))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_s / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_json(cfg),
+        "config": config_json(cfg, args.rope),
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
@@ -381,13 +413,22 @@ def run_ours(args, cfg):
                      "min_ms": min(kernel_ms)},
         "e2e": {"value": whole_job_tflops(flops, e2e_steps, world, e2e_s), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if args.rope else 1),
         "clocks": clocks.summary(t_wall0, t_wall1),
         "wall_s_timed_region": t_wall1 - t_wall0,
         "kernel_source_hash": kernel_source_hash(),
     }
+    if args.rope:
+        kv_bytes = 2 * cfg.B * cfg.Sk * cfg.Hkv * cfg.D * 2          # read K, write rotated K
+        med = statistics.median(key_ms)
+        hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        line["key_rotation"] = {"kernel": "rope_apply_kernel", "median_ms": med, "bytes": kv_bytes,
+                                "achieved_gbs": kv_bytes / (med / 1e3) / 1e9, "peak_gbs": hbm,
+                                "frac": kv_bytes / (med / 1e3) / 1e9 / hbm,
+                                "share_of_step": sum(key_ms) / sum(step_ms)}
     if world == 1 and not args.no_cpu_baseline:
-        sec, done, n, threads = oracle_sample(cfg, q, k, v, mask, args.cpu_seconds, spread_slices(cfg))
+        rope_kw = dict(rope_base=ROPE_BASE, rope_round=True) if args.rope else None
+        sec, done, n, threads = oracle_sample(cfg, q, k, v, mask, args.cpu_seconds, spread_slices(cfg), rope_kw)
         line["cpu_baseline"] = {"value": done / sec / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                                 "sample": f"{n} of {cfg.B * cfg.Hq} (b,h) slices, all rows, "
                                           f"{sec:.1f} s of FP64 oracle time"}
@@ -404,6 +445,8 @@ def main(argv=None):
     ap.add_argument("--config", default=I.BENCH_CONFIG, choices=sorted(I.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rope", action="store_true",
+                    help="rotary position embedding: keys rotated once per step, queries inside the kernel")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

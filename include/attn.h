@@ -187,6 +187,74 @@ int attn_fwd_splitkv_noalloc(const void *q, const void *k, const void *v, void *
                              attn_stream_t stream);
 
 /*
+ * Rotary position embedding (RoPE) fused with the attention: [GUIDE] §4.1
+ * fusion pattern 5 (RoPE(Q) + RoPE(K) + attention as one operation, no
+ * rotated temporaries) and §8.4 (interleaved pairs, rotary base 10000,
+ * fuse_with_attention). The pair (x[2i], x[2i+1]) of a head vector at
+ * position pos turns by the angle pos * base^(-2i/D):
+ *     (x[2i], x[2i+1]) -> (x[2i] cos - x[2i+1] sin, x[2i+1] cos + x[2i] sin).
+ * The rotated vectors are rounded to the input's 16-bit type (the type the
+ * tensor cores read), as the reference rotation of §8.4 returns them.
+ *
+ * attn_rope_table — fills `table` (device, FP32, max_pos x D/2 x 2,
+ * 16-byte aligned, caller-owned) with {cos, sin} of pos * base^(-2i/D) for
+ * pos < max_pos, i < D/2, evaluated in double and rounded to FP32. D even,
+ * base > 1, max_pos * D <= 2^31. Build it once per (max_pos, D, base) and
+ * pass it to the calls below.
+ */
+int attn_rope_table(float *table, int max_pos, int D, double base, attn_stream_t stream);
+
+/*
+ * attn_rope_apply / attn_rope_apply_f16 — rotate every head vector of the
+ * (B, S, H, D) 16-bit tensor x (device, 16-byte aligned) into y (same shape,
+ * may equal x: in place); row s is at position pos0 + s. D a multiple of 8;
+ * pos0 >= 0 and pos0 + S <= max_pos. For keys written once into a cache and
+ * read by many later calls (the cache then holds rotated keys).
+ * Bandwidth-bound: one read and one write of x.
+ */
+int attn_rope_apply(const void *x, void *y, int B, int S, int H, int D,
+                    const float *rope_table, int max_pos, int pos0, attn_stream_t stream);
+int attn_rope_apply_f16(const void *x, void *y, int B, int S, int H, int D,
+                        const float *rope_table, int max_pos, int pos0, attn_stream_t stream);
+
+/*
+ * attn_fwd_rope / attn_fwd_rope_f16 — attention of the rotated queries and
+ * keys: O = softmax(scale * rot(Q) rot(K)^T + mask) V, with query row i at
+ * position q_pos0 + i and key j at k_pos0 + j.
+ *
+ * The queries are rotated inside the attention kernel, after each Q tile's
+ * load lands in shared memory and before the tensor cores read it; no rotated
+ * copy of Q exists. The keys are rotated once per key: on GB300 a 128 x D key
+ * tile takes the tensor cores 256 cycles (D = 128) to use but over a thousand
+ * warp instructions to rotate, and every query tile of the head would repeat
+ * it, so rotating keys at tile load would make the kernel ALU-bound. Hence:
+ *   k_rot   device buffer of k's shape and layout (16-byte aligned) that
+ *           receives rot(K) from a bandwidth-bound pass enqueued before the
+ *           attention kernel (k_rot may equal k: the keys are then rotated in
+ *           place); or NULL: k already holds rotated keys (a KV cache filled
+ *           through attn_rope_apply) and k_pos0 is not used. k_rot is written
+ *           only when there is output to compute (B, Hq, Sq, Sk all > 0). It
+ *           must not overlap q, v, o, lse or mask.
+ *   rope_table, max_pos  the table of attn_rope_table, built for this D;
+ *           q_pos0 >= 0 and q_pos0 + Sq <= max_pos; with k_rot, also
+ *           k_pos0 >= 0 and k_pos0 + Sk <= max_pos.
+ *   num_splits, workspace, workspace_bytes  as for attn_fwd_splitkv
+ *           (num_splits = 1 with a NULL workspace: one pass, no split).
+ * Other arguments, results and errors as for attn_fwd_splitkv /
+ * attn_fwd_splitkv_f16; bad rotary arguments are ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_rope(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                  float scale, int mask_kind, const float *mask,
+                  const float *rope_table, int max_pos, int q_pos0, int k_pos0, void *k_rot,
+                  int num_splits, void *workspace, size_t workspace_bytes, attn_stream_t stream);
+int attn_fwd_rope_f16(const void *q, const void *k, const void *v, void *o, float *lse,
+                      int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                      float scale, int mask_kind, const float *mask,
+                      const float *rope_table, int max_pos, int q_pos0, int k_pos0, void *k_rot,
+                      int num_splits, void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * attn_last_status — synchronises `stream`, then returns and clears the
  * current device's run-time status word: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT
  * if any launch since the last call gave up on a bounded wait (the kernel then

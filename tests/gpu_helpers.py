@@ -30,8 +30,14 @@ def run_gpu(q, k, v, mask, causal, scale=None, device="cuda"):
 
 
 def check(o_gpu, lse_gpu, q, k, v, mask, mask_kind, *, scale=None, slices=None, rows=None,
-          heavy_tail=False, label=""):
-    """Compare GPU outputs with the oracle on the given (b, h) slices and rows."""
+          heavy_tail=False, label="", rope=None):
+    """Compare GPU outputs with the oracle on the given (b, h) slices and rows.
+
+    rope: None, or dict(base=, q_pos0=, k_pos0=) for the rotary variant (the
+    oracle then rotates q and k and holds them in the input's 16-bit type).
+    """
+    rope_kw = {} if rope is None else dict(rope_base=rope["base"], q_pos0=rope["q_pos0"],
+                                           k_pos0=rope["k_pos0"], rope_round=True)
     B, Sq, Hq, D = q.shape
     if slices is None:
         slices = [(b, h) for b in range(B) for h in range(Hq)]
@@ -39,7 +45,7 @@ def check(o_gpu, lse_gpu, q, k, v, mask, mask_kind, *, scale=None, slices=None, 
     ref_o, ref_l = oracle.default().attention(
         I.bits(q), I.bits(k), I.bits(v), mask_kind=mask_kind,
         mask=None if mask is None else mask.numpy(), scale=scale, slices=slices, rows=(r0, r1),
-        dtype="f16" if q.dtype == torch.float16 else "bf16")
+        dtype="f16" if q.dtype == torch.float16 else "bf16", **rope_kw)
     og = o_gpu.float().cpu()
     lg = lse_gpu.float().cpu()
     got_o = np.stack([og[b, r0:r1, h, :].numpy() for b, h in slices]).astype(np.float64)

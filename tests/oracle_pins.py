@@ -460,6 +460,18 @@ def pin_rope_round_single_key_closed_form(orc):
             assert np.array_equal(o[0, 0], [0.25, -3.0])
 
 
+def pin_rope_rotate_alone(orc):
+    """The rotation on its own equals the pure-Python rotation (exact), and
+    PyTorch's 16-bit conversion of it (rope_round), for bf16 and fp16."""
+    for n, (dt, tdt, pos0) in enumerate((("bf16", torch.bfloat16, 0), ("f16", torch.float16, 77))):
+        x = _rand16((2, 5, 3, 8), 1600 + n, dtype=tdt)
+        exact = _rope_py(x, pos0, 10000.0)
+        _close(orc.rotate(_bits(x), base=10000.0, pos0=pos0, dtype=dt, rope_round=False), exact.numpy(),
+               tol=1e-14, what=f"rotate exact {dt}")
+        got = orc.rotate(_bits(x), base=10000.0, pos0=pos0, dtype=dt, rope_round=True)
+        assert np.array_equal(got, _held_in(exact, dt).numpy()), f"rotate rounded {dt}"
+
+
 ALL_PINS = [
     pin_brute_force, pin_brute_force_f16, pin_widening_exact, pin_sdpa_float64,
     pin_rowsum_one, pin_constant_v, pin_zero_q, pin_causal_row0, pin_shift_invariance,
@@ -467,4 +479,5 @@ ALL_PINS = [
     pin_two_key_closed_form, pin_fully_masked_row, pin_subset_matches_full,
     pin_rope_brute_force, pin_rope_two_dim_closed_form, pin_rope_depends_on_relative_position,
     pin_rope_position_zero_is_identity, pin_rope_round_brute_force, pin_rope_round_single_key_closed_form,
+    pin_rope_rotate_alone,
 ]

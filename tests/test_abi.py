@@ -138,3 +138,68 @@ def _call_split(num_splits=4, ws=P, ws_bytes=1 << 30, **kw):
 ])
 def test_splitkv_arguments_are_checked_before_launch(lib, kw, code):
     assert _call_split(**kw) == code
+
+
+# ------------------------------------------------------- rotary embedding (host only)
+
+def _call_rope(table=P, max_pos=4096, q_pos0=0, k_pos0=0, k_rot=P, num_splits=1, ws=None, ws_bytes=0, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=1, Hq=2, Hkv=2, Sq=16, Sk=64, D=128, scale=0.0, kind=1, mask=None)
+    a.update(kw)
+    return A.attn_fwd_rope(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"],
+                           a["D"], a["scale"], a["kind"], a["mask"], table, max_pos, q_pos0, k_pos0, k_rot,
+                           num_splits, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(table=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(table=P + 8), A.ATTN_ERR_INVALID_ARG),             # table must be 16-byte aligned
+    (dict(max_pos=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(q_pos0=-1), A.ATTN_ERR_INVALID_ARG),
+    (dict(max_pos=20, q_pos0=5), A.ATTN_ERR_INVALID_ARG),    # query rows 5..20 past the table
+    (dict(max_pos=64, k_pos0=1), A.ATTN_ERR_INVALID_ARG),    # keys 1..64 past the table
+    (dict(k_pos0=-2), A.ATTN_ERR_INVALID_ARG),
+    (dict(k_rot=P + 4), A.ATTN_ERR_INVALID_ARG),
+    (dict(num_splits=4, Sk=4096), A.ATTN_ERR_INVALID_ARG),   # a split needs a workspace
+    (dict(D=96), A.ATTN_ERR_UNSUPPORTED),
+    (dict(B=0), A.ATTN_OK),                                  # empty: nothing to do
+])
+def test_rope_arguments_are_checked_before_launch(lib, kw, code):
+    assert _call_rope(**kw) == code
+
+
+def test_rope_without_key_rotation_ignores_the_key_positions(lib):
+    # k_rot NULL: the keys are taken as already rotated and k_pos0 is not
+    # checked, so validation passes and the call gets as far as the device
+    # query (ATTN_ERR_CUDA without a GPU, not ATTN_ERR_INVALID_ARG)
+    assert _call_rope(k_rot=None, k_pos0=-5, max_pos=64) != A.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args,code", [
+    ((P, 4096, 127, 10000.0), A.ATTN_ERR_INVALID_ARG),       # odd D
+    ((P, 4096, 128, 1.0), A.ATTN_ERR_INVALID_ARG),           # base must exceed 1
+    ((P, 4096, 128, float("inf")), A.ATTN_ERR_INVALID_ARG),
+    ((P, -1, 128, 10000.0), A.ATTN_ERR_INVALID_ARG),
+    ((P + 4, 4096, 128, 10000.0), A.ATTN_ERR_INVALID_ARG),   # misaligned
+    ((None, 4096, 128, 10000.0), A.ATTN_ERR_INVALID_ARG),
+    ((P, 1 << 24, 256, 10000.0), A.ATTN_ERR_INVALID_ARG),    # more than 2^31 entries
+    ((None, 0, 128, 10000.0), A.ATTN_OK),                     # empty table: nothing to do
+])
+def test_rope_table_arguments(lib, args, code):
+    assert A.attn_rope_table(*args, None) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=100), A.ATTN_ERR_INVALID_ARG),                   # D must be a multiple of 8
+    (dict(pos0=-1), A.ATTN_ERR_INVALID_ARG),
+    (dict(S=100, max_pos=99), A.ATTN_ERR_INVALID_ARG),
+    (dict(x=P + 2), A.ATTN_ERR_INVALID_ARG),
+    (dict(y=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(table=P + 8), A.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), A.ATTN_OK),
+    (dict(S=0, pos0=4096), A.ATTN_OK),
+])
+def test_rope_apply_arguments(lib, kw, code):
+    a = dict(x=P, y=P, B=2, S=64, H=4, D=128, table=P, max_pos=4096, pos0=0)
+    a.update(kw)
+    for fn in (A.attn_rope_apply, A.attn_rope_apply_f16):
+        assert fn(a["x"], a["y"], a["B"], a["S"], a["H"], a["D"], a["table"], a["max_pos"], a["pos0"], None) == code

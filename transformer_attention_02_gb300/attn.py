@@ -50,6 +50,15 @@ def lib() -> ctypes.CDLL:
     for f in (L.attn_fwd_splitkv, L.attn_fwd_splitkv_f16):
         f.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P, ctypes.c_size_t, P]
         f.restype = I
+    for f in (L.attn_fwd_rope, L.attn_fwd_rope_f16):
+        f.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, P, I, I, I, P, I, P,
+                      ctypes.c_size_t, P]
+        f.restype = I
+    for f in (L.attn_rope_apply, L.attn_rope_apply_f16):
+        f.argtypes = [P, P, I, I, I, I, P, I, I, P]
+        f.restype = I
+    L.attn_rope_table.argtypes = [P, I, I, ctypes.c_double, P]
+    L.attn_rope_table.restype = I
     L.attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]
     L.attn_fwd_splitkv_noalloc.restype = I
     L.attn_splitkv_num_splits.argtypes = [I, I, I, I, I]
@@ -97,6 +106,30 @@ def attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask
     """The allocation-free split-key entry point (bf16): its scratch is the library's fixed 32 MiB array."""
     return lib().attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
                                           num_splits, stream)
+
+
+def attn_fwd_rope(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, rope_table, max_pos, q_pos0,
+                  k_pos0, k_rot, num_splits, workspace, workspace_bytes, stream) -> int:
+    return lib().attn_fwd_rope(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, rope_table, max_pos,
+                               q_pos0, k_pos0, k_rot, num_splits, workspace, workspace_bytes, stream)
+
+
+def attn_fwd_rope_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, rope_table, max_pos, q_pos0,
+                      k_pos0, k_rot, num_splits, workspace, workspace_bytes, stream) -> int:
+    return lib().attn_fwd_rope_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, rope_table,
+                                   max_pos, q_pos0, k_pos0, k_rot, num_splits, workspace, workspace_bytes, stream)
+
+
+def attn_rope_table(table, max_pos, D, base, stream) -> int:
+    return lib().attn_rope_table(table, max_pos, D, float(base), stream)
+
+
+def attn_rope_apply(x, y, B, S, H, D, rope_table, max_pos, pos0, stream) -> int:
+    return lib().attn_rope_apply(x, y, B, S, H, D, rope_table, max_pos, pos0, stream)
+
+
+def attn_rope_apply_f16(x, y, B, S, H, D, rope_table, max_pos, pos0, stream) -> int:
+    return lib().attn_rope_apply_f16(x, y, B, S, H, D, rope_table, max_pos, pos0, stream)
 
 
 def attn_splitkv_num_splits(B, Hq, Sq, Sk, num_splits=0) -> int:
@@ -212,3 +245,86 @@ def attention_splitkv(q, k, v, *, causal: bool = False, mask=None, scale=None, n
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_splitkv")
     return out, lse
+
+
+def rope_table(max_pos: int, D: int, base: float = 10000.0, *, device=None, stream=None):
+    """FP32 (max_pos, D/2, 2) table of {cos, sin}(pos * base^(-2i/D)), built on the GPU."""
+    import torch
+    table = torch.empty((max_pos, D // 2, 2), dtype=torch.float32, device=device or "cuda")
+    rc = attn_rope_table(table.data_ptr(), max_pos, D, base, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_rope_table")
+    return table
+
+
+def rope_apply(x, table, *, pos0: int = 0, out=None, stream=None):
+    """Rotate every head vector of a (B, S, H, D) bf16/fp16 CUDA tensor (row s at
+    position pos0 + s) into `out` (new tensor by default; may be x itself)."""
+    import torch
+    if x.dtype not in (torch.bfloat16, torch.float16) or not (x.is_cuda and x.dim() == 4 and x.is_contiguous()):
+        raise ValueError("x must be a contiguous 4-D bf16/fp16 CUDA tensor (B, S, H, D)")
+    if out is None:
+        out = torch.empty_like(x)
+    B, S, H, D = x.shape
+    fn = attn_rope_apply if x.dtype == torch.bfloat16 else attn_rope_apply_f16
+    rc = fn(x.data_ptr(), out.data_ptr(), B, S, H, D, table.data_ptr(), table.shape[0], int(pos0),
+            _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_rope_apply")
+    return out
+
+
+def attention_rope(q, k, v, table, *, q_pos0: int = 0, k_pos0: int = 0, k_rot="new", causal: bool = False,
+                   mask=None, scale=None, num_splits: int = 1, workspace=None, out=None, lse=None, stream=None):
+    """attention(rot(Q), rot(K), V) with the rotary table of rope_table().
+
+    Q is rotated inside the attention kernel at tile load. k_rot: "new" (a
+    tensor allocated here receives the rotated keys), a tensor of k's shape
+    (may be k itself: rotated in place), or None (k already holds rotated
+    keys). num_splits / workspace as for attention_splitkv (1: no split).
+    Returns (out, lse) or, when the keys were rotated here, (out, lse, k_rot).
+    """
+    import torch
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v must be bf16 or fp16")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (t.is_cuda and t.dtype == q.dtype and t.dim() == 4 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor (B, S, H, D) of q's dtype")
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or v.shape != k.shape:
+        raise ValueError("q, k, v shapes disagree")
+    if not (table.is_cuda and table.dtype == torch.float32 and table.dim() == 3 and table.shape[1:] == (D // 2, 2)
+            and table.is_contiguous()):
+        raise ValueError("table must be the (max_pos, D/2, 2) FP32 CUDA tensor of rope_table() for this D")
+    if isinstance(k_rot, str):
+        if k_rot != "new":
+            raise ValueError("k_rot must be 'new', a tensor of k's shape, or None")
+        k_rot = torch.empty_like(k)
+    if k_rot is not None and not (k_rot.is_cuda and k_rot.dtype == k.dtype and k_rot.shape == k.shape
+                                  and k_rot.is_contiguous()):
+        raise ValueError("k_rot must be a contiguous CUDA tensor of k's shape and dtype")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    need = attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    kind = (MASK_CAUSAL if causal else MASK_NONE) + (MASK_ADDITIVE if mask is not None else 0)
+    mptr = None
+    if mask is not None:
+        if not (mask.is_cuda and mask.dtype == torch.float32 and mask.is_contiguous()
+                and tuple(mask.shape) == (B, Sq, Sk)):
+            raise ValueError("mask must be a contiguous FP32 CUDA tensor of shape (B, Sq, Sk)")
+        mptr = mask.data_ptr()
+    sc = float("nan") if scale is None else float(scale)
+    fn = attn_fwd_rope if q.dtype == torch.bfloat16 else attn_fwd_rope_f16
+    rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D,
+            sc, kind, mptr, table.data_ptr(), table.shape[0], int(q_pos0), int(k_pos0),
+            None if k_rot is None else k_rot.data_ptr(), int(num_splits),
+            None if workspace is None else workspace.data_ptr(),
+            0 if workspace is None else workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_rope")
+    return (out, lse) if k_rot is None else (out, lse, k_rot)

@@ -20,10 +20,11 @@
 
 #include "../../include/attn.h"
 #include "attn_kernel.cuh"
+#include "attn_launch.h"
 
 namespace {
 
-constexpr int kAbiVersion = 3;
+constexpr int kAbiVersion = 4;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 constexpr int kMaxDevices = 64;
 
@@ -38,7 +39,7 @@ struct DeviceInfo {
     bool supported = false;
     int num_sms = 0;
     unsigned int* status = nullptr;     // device address of g_device_status
-    bool smem_attr_set[2][4][2] = {};   // [D is 128][mask kind][bf16]
+    bool smem_attr_set[2][4][2][2] = {};   // [D is 128][mask kind][bf16][rotary]
 };
 
 std::mutex g_mutex;
@@ -152,33 +153,73 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
     if (lane == 0) lse[row] = total > 0.f ? m + logf(total) : -INFINITY;
 }
 
-template <int D, bool CAUSAL, bool ADDITIVE, bool BF16>
-int launch_one(DeviceInfo& dev, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const attn::FwdParams& p, int grid, cudaStream_t stream) {
-    auto kernel = attn::attn_fwd_kernel<D, CAUSAL, ADDITIVE, BF16>;
-    constexpr int smem = attn::TileCfg<D>::kSmemBytes;
-    bool& attr = dev.smem_attr_set[D == 128][(CAUSAL ? 1 : 0) + (ADDITIVE ? 2 : 0)][BF16 ? 1 : 0];
-    if (!attr) {
-        // The in-kernel register split assumes exactly kLaunchRegs per thread at launch.
-        cudaFuncAttributes fa{};
-        if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return ATTN_ERR_CUDA;
-        if (fa.numRegs != attn::kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
-        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return ATTN_ERR_CUDA;
-        attr = true;
-    }
-    kernel<<<grid, attn::kThreads, smem, stream>>>(tq, tk, tv, p);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
-template <int D, bool BF16>
+template <int D, bool BF16, bool ROPE>
 int launch_d(DeviceInfo& dev, int mask_kind, const CUtensorMap& tq, const CUtensorMap& tk,
              const CUtensorMap& tv, const attn::FwdParams& p, int grid, cudaStream_t stream) {
+    bool* attr = dev.smem_attr_set[D == 128][mask_kind][BF16 ? 1 : 0] + (ROPE ? 1 : 0);
     switch (mask_kind) {
-        case ATTN_MASK_NONE: return launch_one<D, false, false, BF16>(dev, tq, tk, tv, p, grid, stream);
-        case ATTN_MASK_CAUSAL: return launch_one<D, true, false, BF16>(dev, tq, tk, tv, p, grid, stream);
-        case ATTN_MASK_ADDITIVE: return launch_one<D, false, true, BF16>(dev, tq, tk, tv, p, grid, stream);
-        default: return launch_one<D, true, true, BF16>(dev, tq, tk, tv, p, grid, stream);
+        case ATTN_MASK_NONE: return attn::launch_fwd<D, false, false, BF16, ROPE>(*attr, tq, tk, tv, p, grid, stream);
+        case ATTN_MASK_CAUSAL: return attn::launch_fwd<D, true, false, BF16, ROPE>(*attr, tq, tk, tv, p, grid, stream);
+        case ATTN_MASK_ADDITIVE: return attn::launch_fwd<D, false, true, BF16, ROPE>(*attr, tq, tk, tv, p, grid, stream);
+        default: return attn::launch_fwd<D, true, true, BF16, ROPE>(*attr, tq, tk, tv, p, grid, stream);
+    }
+}
+
+template <bool BF16, bool ROPE>
+int launch_any(DeviceInfo& dev, int D, int mask_kind, const CUtensorMap& tq, const CUtensorMap& tk,
+               const CUtensorMap& tv, const attn::FwdParams& p, int grid, cudaStream_t stream) {
+    return D == 128 ? launch_d<128, BF16, ROPE>(dev, mask_kind, tq, tk, tv, p, grid, stream)
+                    : launch_d<64, BF16, ROPE>(dev, mask_kind, tq, tk, tv, p, grid, stream);
+}
+
+// ------------------------------------------------ rotary position embedding
+// Table of the rotation angles (max_pos, D/2, {cos, sin}) in FP32: entry
+// (pos, i) holds cos and sin of pos * base^(-2i/D), computed in double.
+__global__ void rope_table_kernel(float* table, int max_pos, int D, double base) {
+    const long long n = (long long)max_pos * (D / 2);
+    for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (long long)gridDim.x * blockDim.x) {
+        const long long pos = e / (D / 2);
+        const int i = (int)(e % (D / 2));
+        double sn, cs;
+        sincos((double)pos * pow(base, -2.0 * i / D), &sn, &cs);
+        table[2 * e] = (float)cs;
+        table[2 * e + 1] = (float)sn;
+    }
+}
+
+// Rotates every head vector of a (B, S, H, D) 16-bit tensor: row s sits at
+// position pos0 + s. Each thread moves 16-byte chunks (four pairs), kUnroll of
+// them in flight; y may equal x. Bandwidth-bound: one read and one write of
+// the tensor plus the table rows it touches (L2-resident).
+template <bool BF16>
+__global__ void __launch_bounds__(256) rope_apply_kernel(const uint4* x, uint4* y, long long n_chunks, int S, int H,
+                                                         int D, const float4* table, int pos0) {
+    constexpr int kUnroll = 4;
+    const int chunks_per_row = D / 8;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long c0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; c0 < n_chunks; c0 += stride * kUnroll) {
+        uint4 w[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const long long c = c0 + u * stride;
+            if (c < n_chunks) w[u] = x[c];
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const long long c = c0 + u * stride;
+            if (c >= n_chunks) break;
+            const long long row = c / chunks_per_row;           // (b, s, h) flattened
+            const int g = (int)(c % chunks_per_row);
+            const long long pos = pos0 + (row / H) % S;
+            const float4* cs = table + pos * (D / 4) + 2 * g;
+            const float4 t0 = cs[0], t1 = cs[1];
+            uint4 r;
+            r.x = attn::rotate_pair<BF16>(w[u].x, t0.x, t0.y);
+            r.y = attn::rotate_pair<BF16>(w[u].y, t0.z, t0.w);
+            r.z = attn::rotate_pair<BF16>(w[u].z, t1.x, t1.y);
+            r.w = attn::rotate_pair<BF16>(w[u].w, t1.z, t1.w);
+            y[c] = r;
+        }
     }
 }
 
@@ -223,9 +264,35 @@ size_t workspace_layout(int B, int Hq, int Sq, int D, int splits, size_t* lse_of
     return *lse_off + (size_t)splits * rows * sizeof(float);
 }
 
+// Rotary embedding arguments of attn_fwd_rope / attn_fwd_rope_f16.
+struct RopeArgs {
+    const float* table;   // (max_pos, D/2, {cos, sin}) FP32
+    int max_pos;
+    int q_pos0, k_pos0;   // positions of query row 0 and key 0
+    void* k_rot;          // receives the rotated keys, or null: k already holds rotated keys
+};
+
+bool rope_args_ok(const RopeArgs& r, int Sq, int Sk) {
+    if (!r.table || !aligned(r.table, 16) || r.max_pos <= 0) return false;
+    if (r.q_pos0 < 0 || (long long)r.q_pos0 + Sq > r.max_pos) return false;
+    if (r.k_rot) {
+        if (r.k_pos0 < 0 || (long long)r.k_pos0 + Sk > r.max_pos) return false;
+        if (!aligned(r.k_rot, 16)) return false;
+    }
+    return true;
+}
+
+// Grid of a bandwidth-bound element-wise kernel: enough 256-thread blocks to
+// cover the work, at most 8 per SM.
+unsigned elementwise_grid(long long work, int num_sms) {
+    const long long blocks = (work + 255) / 256;
+    return (unsigned)std::max(1LL, std::min(blocks, 8LL * num_sms));
+}
+
 int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                   int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, cudaStream_t stream,
-                  bool bf16, int num_splits = 1, void* workspace = nullptr, size_t workspace_bytes = 0) {
+                  bool bf16, int num_splits = 1, void* workspace = nullptr, size_t workspace_bytes = 0,
+                  const RopeArgs* rope = nullptr) {
     // ---- arguments (host only, nothing enqueued yet)
     if (B < 0 || Hq < 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_ADDITIVE) return ATTN_ERR_INVALID_ARG;
@@ -241,6 +308,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
         return ATTN_ERR_INVALID_ARG;
     if (additive && !aligned(mask, 4)) return ATTN_ERR_INVALID_ARG;
     if (Sq > (1 << 30) || Sk > (1 << 30)) return ATTN_ERR_INVALID_ARG;
+    if (rope && !rope_args_ok(*rope, Sq, Sk)) return ATTN_ERR_INVALID_ARG;
     const long long n_mblk = ((long long)Sq + attn::kRowsPerTile - 1) / attn::kRowsPerTile;
     if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
     int split_blocks = 1;
@@ -262,6 +330,20 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
         const size_t n_o = (size_t)B * Sq * Hq * D, n_lse = (size_t)B * Hq * Sq;
         fill_empty_rows_kernel<<<dev->num_sms, 256, 0, stream>>>(static_cast<uint16_t*>(o), n_o, lse, n_lse);
         return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    }
+
+    if (rope && rope->k_rot) {                               // rotate each key once
+        const long long n_chunks = (long long)B * Sk * Hkv * (D / 8);
+        const unsigned g = elementwise_grid(n_chunks, dev->num_sms);
+        const auto* table = reinterpret_cast<const float4*>(rope->table);
+        if (bf16)
+            rope_apply_kernel<true><<<g, 256, 0, stream>>>(static_cast<const uint4*>(k), static_cast<uint4*>(rope->k_rot),
+                                                           n_chunks, Sk, Hkv, D, table, rope->k_pos0);
+        else
+            rope_apply_kernel<false><<<g, 256, 0, stream>>>(static_cast<const uint4*>(k), static_cast<uint4*>(rope->k_rot),
+                                                            n_chunks, Sk, Hkv, D, table, rope->k_pos0);
+        if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+        k = rope->k_rot;
     }
 
     CUtensorMap tq, tk, tv;
@@ -293,14 +375,16 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     p.debug_stall = g_debug_stall.load();
     p.timeout_ns = g_timeout_ns.load();
     p.status = dev->status;
+    p.rope = rope ? rope->table : nullptr;
+    p.q_pos0 = rope ? rope->q_pos0 : 0;
 
     const int grid = p.n_tiles < dev->num_sms ? p.n_tiles : dev->num_sms;
-    if (D == 128)
-        rc = bf16 ? launch_d<128, true>(*dev, mask_kind, tq, tk, tv, p, grid, stream)
-                  : launch_d<128, false>(*dev, mask_kind, tq, tk, tv, p, grid, stream);
+    if (rope)
+        rc = bf16 ? launch_any<true, true>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
+                  : launch_any<false, true>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);
     else
-        rc = bf16 ? launch_d<64, true>(*dev, mask_kind, tq, tk, tv, p, grid, stream)
-                  : launch_d<64, false>(*dev, mask_kind, tq, tk, tv, p, grid, stream);
+        rc = bf16 ? launch_any<true, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
+                  : launch_any<false, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);
     if (rc != ATTN_OK || splits == 1) return rc;
 
     // ---- merge the key ranges
@@ -360,6 +444,77 @@ int attn_fwd_splitkv_f16(const void* q, const void* k, const void* v, void* o, f
                          void* workspace, size_t workspace_bytes, attn_stream_t stream) {
     return attn_fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
                          reinterpret_cast<cudaStream_t>(stream), false, num_splits, workspace, workspace_bytes);
+}
+
+int attn_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Sq,
+                  int Sk, int D, float scale, int mask_kind, const float* mask, const float* rope_table, int max_pos,
+                  int q_pos0, int k_pos0, void* k_rot, int num_splits, void* workspace, size_t workspace_bytes,
+                  attn_stream_t stream) {
+    const RopeArgs r{rope_table, max_pos, q_pos0, k_pos0, k_rot};
+    return attn_fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
+                         reinterpret_cast<cudaStream_t>(stream), true, num_splits, workspace, workspace_bytes, &r);
+}
+
+int attn_fwd_rope_f16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                      int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, const float* rope_table,
+                      int max_pos, int q_pos0, int k_pos0, void* k_rot, int num_splits, void* workspace,
+                      size_t workspace_bytes, attn_stream_t stream) {
+    const RopeArgs r{rope_table, max_pos, q_pos0, k_pos0, k_rot};
+    return attn_fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask,
+                         reinterpret_cast<cudaStream_t>(stream), false, num_splits, workspace, workspace_bytes, &r);
+}
+
+int attn_rope_table(float* table, int max_pos, int D, double base, attn_stream_t stream) {
+    if (max_pos < 0 || D <= 0 || D % 2 != 0 || !(base > 1.0) || !std::isfinite(base)) return ATTN_ERR_INVALID_ARG;
+    if ((long long)max_pos * D > (1LL << 31)) return ATTN_ERR_INVALID_ARG;
+    if (max_pos == 0) return ATTN_OK;
+    if (!table || !aligned(table, 16)) return ATTN_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != ATTN_OK) return rc;
+    const long long n = (long long)max_pos * (D / 2);
+    rope_table_kernel<<<elementwise_grid(n, dev->num_sms), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        table, max_pos, D, base);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+int rope_apply_impl(const void* x, void* y, int B, int S, int H, int D, const float* table, int max_pos, int pos0,
+                    cudaStream_t stream, bool bf16) {
+    if (B < 0 || S < 0 || H < 0 || D <= 0 || D % 8 != 0 || max_pos < 0 || pos0 < 0) return ATTN_ERR_INVALID_ARG;
+    if ((long long)pos0 + S > max_pos) return ATTN_ERR_INVALID_ARG;
+    const long long n_chunks = (long long)B * S * H * (D / 8);
+    if (n_chunks == 0) return ATTN_OK;
+    if (!x || !y || !table || !aligned(x, 16) || !aligned(y, 16) || !aligned(table, 16)) return ATTN_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != ATTN_OK) return rc;
+    const unsigned g = elementwise_grid(n_chunks, dev->num_sms);
+    const auto* t4 = reinterpret_cast<const float4*>(table);
+    if (bf16)
+        rope_apply_kernel<true><<<g, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<uint4*>(y), n_chunks, S, H,
+                                                       D, t4, pos0);
+    else
+        rope_apply_kernel<false><<<g, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<uint4*>(y), n_chunks, S,
+                                                        H, D, t4, pos0);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_rope_apply(const void* x, void* y, int B, int S, int H, int D, const float* rope_table, int max_pos, int pos0,
+                    attn_stream_t stream) {
+    return rope_apply_impl(x, y, B, S, H, D, rope_table, max_pos, pos0, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+int attn_rope_apply_f16(const void* x, void* y, int B, int S, int H, int D, const float* rope_table, int max_pos,
+                        int pos0, attn_stream_t stream) {
+    return rope_apply_impl(x, y, B, S, H, D, rope_table, max_pos, pos0, reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 }  // extern "C"

@@ -1,0 +1,45 @@
+// Definition of launch_fwd and the macro that instantiates one family of
+// forward-kernel variants (both head dimensions, all four mask kinds) in a
+// translation unit of its own.
+#pragma once
+
+#include "../../include/attn.h"
+#include "attn_kernel.cuh"
+#include "attn_launch.h"
+
+namespace attn {
+
+template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE>
+int launch_fwd(bool& attr_set, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+               const FwdParams& p, int grid, cudaStream_t stream) {
+    auto kernel = attn_fwd_kernel<D, CAUSAL, ADDITIVE, BF16, ROPE>;
+    constexpr int smem = TileCfg<D>::kSmemBytes;
+    if (!attr_set) {
+        // The in-kernel register split assumes exactly kLaunchRegs per thread at launch.
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return ATTN_ERR_CUDA;
+        if (fa.numRegs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        attr_set = true;
+    }
+    kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace attn
+
+#define ATTN_INSTANTIATE_ONE(D, CAUSAL, ADDITIVE, BF16, ROPE)                                                  \
+    template int attn::launch_fwd<D, CAUSAL, ADDITIVE, BF16, ROPE>(bool&, const CUtensorMap&,                  \
+                                                                   const CUtensorMap&, const CUtensorMap&,     \
+                                                                   const attn::FwdParams&, int, cudaStream_t);
+
+#define ATTN_INSTANTIATE_FWD(BF16, ROPE)                  \
+    ATTN_INSTANTIATE_ONE(64, false, false, BF16, ROPE)    \
+    ATTN_INSTANTIATE_ONE(64, true, false, BF16, ROPE)     \
+    ATTN_INSTANTIATE_ONE(64, false, true, BF16, ROPE)     \
+    ATTN_INSTANTIATE_ONE(64, true, true, BF16, ROPE)      \
+    ATTN_INSTANTIATE_ONE(128, false, false, BF16, ROPE)   \
+    ATTN_INSTANTIATE_ONE(128, true, false, BF16, ROPE)    \
+    ATTN_INSTANTIATE_ONE(128, false, true, BF16, ROPE)    \
+    ATTN_INSTANTIATE_ONE(128, true, true, BF16, ROPE)

@@ -60,12 +60,15 @@ struct FwdParams {
     int debug_stall;          // wait on a barrier nothing signals (timeout test)
     unsigned long long timeout_ns;
     unsigned int* status;     // device status word, bit 0 = a wait timed out
+    const float* rope;        // rotary table (max_pos, D/2, {cos, sin}) FP32 (rotating variant only)
+    int q_pos0;               // position of query row 0 (rotating variant only)
 };
 
 constexpr int kThreads = 384;               // three warpgroups
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
 constexpr int kQWarp = 10;
+constexpr int kRopeWarp = 11;               // second rotating warp of the rotary variant
 // Register split: launched at 168 per thread (384 x 168 = 64512), then the
 // softmax warpgroups grow to 200 and the MMA/TMA warpgroup shrinks to 104:
 // 128 x (200 + 200 + 104) = 64512. The host refuses to launch unless the
@@ -106,7 +109,8 @@ struct TileCfg {
     static constexpr int bStall = bDrain + 1;
     static constexpr int bKVFull = bStall + 1;        // [kSlots]
     static constexpr int bKVEmpty = bKVFull + kSlots;
-    static constexpr int kNumBars = bKVEmpty + kSlots;
+    static constexpr int bQRdy = bKVEmpty + kSlots;   // [kQBufs] rotary variant: Q sub-tile rotated
+    static constexpr int kNumBars = bQRdy + kQBufs;
     static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemUsed = kAbortOff + 4;
@@ -254,13 +258,109 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
     }
 }
 
+// ------------------------------------------------- rotary position embedding
+// Rotation of the query rows at tile load ("ATB engineering guide" §4.1,
+// fusion pattern 5; interleaved pairs as in its §8.4): the pair
+// (x[2i], x[2i+1]) of the row at position pos turns by the angle of the
+// table's entry (pos, i):
+//   (x[2i], x[2i+1]) -> (x[2i] cos - x[2i+1] sin, x[2i+1] cos + x[2i] sin),
+// in FP32, rounded once to the 16-bit input type the tensor core reads.
+template <bool BF16>
+__device__ __forceinline__ uint32_t rotate_pair(uint32_t w, float c, float s) {
+    float x0, x1;
+    if (BF16) {
+        x0 = __uint_as_float(w << 16);
+        x1 = __uint_as_float(w & 0xffff0000u);
+    } else {
+        asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+            : "=f"(x0), "=f"(x1)
+            : "r"(w));
+    }
+    const float y0 = x0 * c - x1 * s, y1 = x1 * c + x0 * s;
+    return BF16 ? ptx::pack_bf16x2(y0, y1) : ptx::pack_f16x2(y0, y1);
+}
+
+// One warp rotates rows [r_begin, r_end) of a 128 x D sub-tile held as
+// 128-byte-swizzled 64-column boxes; the sub-tile's row r is query row
+// row0 + r. Each lane moves 16 bytes (four pairs) at a time. Rows at or past
+// Sq (zero fill of the load) are skipped. The writes are made visible to the
+// tensor core's (async) proxy before the caller signals.
+template <int D, bool BF16>
+__device__ void rope_rotate_rows(uint8_t* tile, int r_begin, int r_end, int row0, const FwdParams& p) {
+    using C = TileCfg<D>;
+    constexpr int kChunks = D / 8;                 // 16-byte chunks per row
+    constexpr int kRowsPerPass = 32 / kChunks;
+    const int lane = threadIdx.x & 31;
+    const int g = lane % kChunks;                  // chunk of the row: pairs 4g .. 4g+3
+    const int box = g / 8, k = g % 8;
+    const int r_stop = min(r_end, p.Sq - row0);
+    const float4* table = reinterpret_cast<const float4*>(p.rope) + 2 * g;
+#pragma unroll 4
+    for (int r = r_begin + lane / kChunks; r < r_stop; r += kRowsPerPass) {
+        uint4* ptr = reinterpret_cast<uint4*>(tile + box * C::kBoxBytes + r * 128 + ((k ^ (r & 7)) << 4));
+        const float4* cs = table + (size_t)(p.q_pos0 + row0 + r) * (D / 4);
+        const float4 t0 = __ldg(cs), t1 = __ldg(cs + 1);      // (c, s) of pairs 4g .. 4g+3
+        uint4 w = *ptr;
+        w.x = rotate_pair<BF16>(w.x, t0.x, t0.y);
+        w.y = rotate_pair<BF16>(w.y, t0.z, t0.w);
+        w.z = rotate_pair<BF16>(w.z, t1.x, t1.y);
+        w.w = rotate_pair<BF16>(w.w, t1.z, t1.w);
+        *ptr = w;
+    }
+    ptx::fence_proxy_async_shared();
+    __syncwarp();
+}
+
+// Next work tile with at least one key block, from wave w0 on.
+template <bool CAUSAL>
+__device__ bool next_work_tile(const FwdParams& p, int w0, int& w_out, TileInfo& t_out) {
+    for (int w = w0; w * (int)gridDim.x < p.n_tiles; ++w) {
+        const int tile = tile_of_wave(w);
+        if (tile >= p.n_tiles) continue;
+        t_out = tile_info<CAUSAL>(tile, p);
+        if (t_out.n == 0) continue;
+        w_out = w;
+        return true;
+    }
+    return false;
+}
+
+// Rotary variant, warp 11: rotates rows 64..127 of every Q sub-tile once its
+// load has landed (the Q warp does rows 0..63), in the order the Q warp loads
+// them, and signals "Q ready" (two arrivals per use).
+template <int D, bool CAUSAL, bool BF16>
+__device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr, const SyncCtx& sc) {
+    using C = TileCfg<D>;
+    const bool leader = (threadIdx.x & 31) == 0;
+    const uint32_t bars = smem + C::kBarOff;
+    auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    uint32_t nq = 0;
+    int w = -1;
+    TileInfo ti;
+    while (next_work_tile<CAUSAL>(p, w + 1, w, ti)) {
+        const int buf[2] = {(int)(nq & 1u), 2 + (int)(nq % C::kQ1Bufs)};
+        const uint32_t use[2] = {nq >> 1, nq / C::kQ1Bufs};
+        for (int t = 0; t < 2; ++t) {
+            if (!warp_wait(bar(C::bQFull + buf[t]), use[t] & 1u, sc)) return;
+            rope_rotate_rows<D, BF16>(smem_ptr + C::kQOff + buf[t] * C::kTileBytes, kBlockM / 2, kBlockM,
+                                      ti.m0 + t * kBlockM, p);
+            if (leader) ptx::mbar_arrive(bar(C::bQRdy + buf[t]));
+        }
+        ++nq;
+    }
+}
+
 // ------------------------------------------------------------- Q producer
 // Loads the Q sub-tiles of each work tile. The lower sub-tile alternates
 // between two buffers, so it is fetched as soon as the tile before the current
 // one has finished with it; the upper sub-tile reuses one buffer and is fetched
-// while the previous tile's last products and epilogue run.
-template <int D, bool CAUSAL>
-__device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t smem, const SyncCtx& sc) {
+// while the previous tile's last products and epilogue run. In the rotary
+// variant this warp also rotates rows 0..63 of each sub-tile after it lands:
+// the lower sub-tile of tile T (loaded during tile T-1) first, then, once the
+// upper buffer is free, the upper one.
+template <int D, bool CAUSAL, bool BF16, bool ROPE>
+__device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t smem, uint8_t* smem_ptr,
+                           const SyncCtx& sc) {
     using C = TileCfg<D>;
     const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
@@ -278,13 +378,40 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
         ++uses[buf];
         return true;
     };
-    for (int w = 0; w * (int)gridDim.x < p.n_tiles; ++w) {
-        const int tile = tile_of_wave(w);
-        if (tile >= p.n_tiles) continue;
-        const TileInfo ti = tile_info<CAUSAL>(tile, p);
-        if (ti.n == 0) continue;
-        if (!load(nq & 1, ti.m0, ti) || !load(2 + nq % C::kQ1Bufs, ti.m0 + kBlockM, ti)) break;
-        ++nq;
+    auto rotate = [&](int buf, uint32_t use, int row0) -> bool {
+        if (!warp_wait(bar(C::bQFull + buf), use & 1u, sc)) return false;
+        rope_rotate_rows<D, BF16>(smem_ptr + C::kQOff + buf * C::kTileBytes, 0, kBlockM / 2, row0, p);
+        if (leader) ptx::mbar_arrive(bar(C::bQRdy + buf));
+        return true;
+    };
+    if (!ROPE) {
+        for (int w = 0; w * (int)gridDim.x < p.n_tiles; ++w) {
+            const int tile = tile_of_wave(w);
+            if (tile >= p.n_tiles) continue;
+            const TileInfo ti = tile_info<CAUSAL>(tile, p);
+            if (ti.n == 0) continue;
+            if (!load(nq & 1, ti.m0, ti) || !load(2 + nq % C::kQ1Bufs, ti.m0 + kBlockM, ti)) break;
+            ++nq;
+        }
+    } else {
+        int w = 0;
+        TileInfo ti;
+        bool have = next_work_tile<CAUSAL>(p, 0, w, ti) && load(0, ti.m0, ti);
+        while (have) {
+            const int b0 = nq & 1, b1 = 2 + nq % C::kQ1Bufs;
+            const bool b1_unused = uses[b1] == 0;       // first use: nothing to wait for
+            if (b1_unused && !load(b1, ti.m0 + kBlockM, ti)) break;
+            if (!rotate(b0, nq >> 1, ti.m0)) break;
+            if (!b1_unused && !load(b1, ti.m0 + kBlockM, ti)) break;
+            if (!rotate(b1, nq / C::kQ1Bufs, ti.m0 + kBlockM)) break;
+            int w_next = 0;
+            TileInfo tn;
+            have = next_work_tile<CAUSAL>(p, w + 1, w_next, tn);
+            if (have && !load((nq + 1) & 1, tn.m0, tn)) break;
+            ++nq;
+            w = w_next;
+            ti = tn;
+        }
     }
     // Shut down: wait until every copy this warp started has landed.
     for (int b = 0; b < C::kQBufs; ++b)
@@ -305,7 +432,7 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
 // O_t and overwrite P_t after it).
 // The whole warp runs the loop with warp-uniform descriptors; lane 0 issues
 // every MMA and every commit (a commit covers the MMAs of its own thread).
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16, bool ROPE>
 __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const SyncCtx& sc) {
     using C = TileCfg<D>;
     const bool leader = (threadIdx.x & 31) == 0;
@@ -322,6 +449,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
     uint32_t p_cnt[2] = {0, 0};
     bool issued = false;
     bool alive = true;
+    constexpr int kQReady = ROPE ? C::bQRdy : C::bQFull;   // Q usable once loaded (and rotated)
 
     auto acquire = [&](uint32_t& slot) -> bool {      // next K or V tile of the ring
         slot = kv_use % C::kSlots;
@@ -379,10 +507,10 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
             commit(C::bQEmpty + q_buf[1]);
         };
         uint32_t ks, vs;
-        if (!warp_wait(bar(C::bQFull + q_buf[0]), (nq >> 1) & 1u, sc) || !acquire(ks)) { alive = false; break; }
+        if (!warp_wait(bar(kQReady + q_buf[0]), (nq >> 1) & 1u, sc) || !acquire(ks)) { alive = false; break; }
         if (n0 > 0) issue_qk(0, ks);
         issued = true;
-        if (!warp_wait(bar(C::bQFull + q_buf[1]), (nq / C::kQ1Bufs) & 1u, sc)) { alive = false; break; }
+        if (!warp_wait(bar(kQReady + q_buf[1]), (nq / C::kQ1Bufs) & 1u, sc)) { alive = false; break; }
         ptx::tc_fence_after_sync();
         ++nq;
         if (n1 > 0) issue_qk(1, ks);
@@ -636,7 +764,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, bool ADDITIVE, bool BF16>
+template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -655,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kTmaWarp && lane == 0) {
         const uint32_t bars = smem + C::kBarOff;
         for (int i = 0; i < C::kNumBars; ++i) {
-            ptx::mbar_init(bars + 8u * i, 1u);
+            ptx::mbar_init(bars + 8u * i, (i >= C::bQRdy && i < C::bQRdy + C::kQBufs) ? 2u : 1u);
         }
         *abort_flag = 0u;
         ptx::fence_barrier_init();
@@ -680,11 +808,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         ptx::setmaxnreg_dec<kControlRegs>();
         if (warp == kMmaWarp)
-            role_mma<D, CAUSAL, BF16>(p, smem, tmem, sc);
+            role_mma<D, CAUSAL, BF16, ROPE>(p, smem, tmem, sc);
         else if (warp == kTmaWarp)
             role_tma<D, CAUSAL>(&tmQ, &tmK, &tmV, p, smem, sc);
         else if (warp == kQWarp)
-            role_qload<D, CAUSAL>(&tmQ, p, smem, sc);
+            role_qload<D, CAUSAL, BF16, ROPE>(&tmQ, p, smem, smem_ptr, sc);
+        else if (ROPE && warp == kRopeWarp)
+            role_rope_q<D, CAUSAL, BF16>(p, smem, smem_ptr, sc);
         __syncwarp();
     }
 
