@@ -56,6 +56,9 @@ class Oracle:
                       I, P, P, I, I, P, P, P, I, ctypes.c_double, ctypes.c_longlong, ctypes.c_longlong, I]
         f.restype = I
         self._lib.oracle_num_threads.restype = I
+        r = self._lib.oracle_rope_rotate
+        r.argtypes = [P, I, I, I, I, I, ctypes.c_double, ctypes.c_longlong, I, P]
+        r.restype = I
 
     def num_threads(self) -> int:
         return int(self._lib.oracle_num_threads())
@@ -113,6 +116,19 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle rejected its arguments (rc={rc})")
         return (o, lse, psum) if want_psum else (o, lse)
+
+    def rotate(self, x, *, base: float, pos0: int = 0, dtype: str = "bf16", rope_round: bool = True):
+        """Rotary embedding alone: x (B, S, H, D) 16-bit bit patterns, row s at
+        position pos0 + s; returns the rotated values as float64, same shape
+        (rounded to `dtype` when rope_round)."""
+        x = np.ascontiguousarray(np.asarray(x).view(np.uint16))
+        B, S, H, D = x.shape
+        y = np.zeros(x.shape, dtype=np.float64)
+        rc = self._lib.oracle_rope_rotate(x.ctypes.data, DTYPES[dtype], B, S, H, D, float(base), int(pos0),
+                                          int(bool(rope_round)), y.ctypes.data)
+        if rc != 0:
+            raise ValueError(f"oracle rejected its arguments (rc={rc})")
+        return y
 
 
 def to_bshd(o_slices: np.ndarray, B: int, Hq: int) -> np.ndarray:

@@ -257,6 +257,25 @@ int oracle_attn_fwd_rope(const uint16_t *q, const uint16_t *k, const uint16_t *v
     return 0;
 }
 
+/*
+ * The rotation alone (for checking a rotation kernel): x is a (B, S, H, D)
+ * tensor of 16-bit patterns, row s at position pos0 + s; y receives the
+ * rotated (and, with rope_round, re-rounded) values in FP64, same layout.
+ * Returns 0, or -1 on an invalid argument.
+ */
+int oracle_rope_rotate(const uint16_t *x, int dtype, int B, int S, int H, int D, double base,
+                       long long pos0, int rope_round, double *y) {
+    if (!x || !y || B < 0 || S < 0 || H < 0 || D <= 0 || D % 2 != 0 || !(base > 0.0)) return -1;
+    for (long long b = 0; b < B; ++b)
+        for (long long s = 0; s < S; ++s)
+            for (long long h = 0; h < H; ++h) {
+                const size_t off = (((size_t)b * S + s) * H + h) * D;
+                for (int d = 0; d < D; ++d) y[off + d] = widen(x[off + d], dtype);
+                rope_rotate(y + off, D, pos0 + s, base, rope_round, dtype);
+            }
+    return 0;
+}
+
 int oracle_attn_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v, int dtype,
                     const float *mask, int mask_kind,
                     int B, int Hq, int Hkv, int Sq, int Sk, int D, double scale,
