@@ -188,37 +188,53 @@ __global__ void rope_table_kernel(float* table, int max_pos, int D, double base)
 }
 
 // Rotates every head vector of a (B, S, H, D) 16-bit tensor: row s sits at
-// position pos0 + s. Each thread moves 16-byte chunks (four pairs), kUnroll of
-// them in flight; y may equal x. Bandwidth-bound: one read and one write of
-// the tensor plus the table rows it touches (L2-resident).
+// position pos0 + s; y may equal x. One warp per token (b, s): its H*D/8
+// 16-byte chunks (four pairs each) are contiguous, and when D/8 divides 32 a
+// lane always meets the same chunk of the head vector, so it fetches its two
+// table entries (L2-resident) once per token. kUnroll chunks are loaded
+// before any is stored, to keep bytes in flight (loads and stores may alias).
+// Bandwidth-bound: one read and one write of the tensor.
 template <bool BF16>
-__global__ void __launch_bounds__(256) rope_apply_kernel(const uint4* x, uint4* y, long long n_chunks, int S, int H,
-                                                         int D, const float4* table, int pos0) {
+__global__ void __launch_bounds__(256) rope_apply_kernel(const uint4* x, uint4* y, long long n_tokens, int S,
+                                                         int chunks_per_token, int chunks_per_row,
+                                                         const float4* table, int pos0) {
     constexpr int kUnroll = 4;
-    const int chunks_per_row = D / 8;
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long c0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; c0 < n_chunks; c0 += stride * kUnroll) {
-        uint4 w[kUnroll];
-#pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const long long c = c0 + u * stride;
-            if (c < n_chunks) w[u] = x[c];
+    const int lane = threadIdx.x & 31;
+    const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
+    const bool fixed_chunk = (32 % chunks_per_row) == 0;
+    for (long long t = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < n_tokens; t += n_warps) {
+        const float4* row = table + (long long)(pos0 + (int)(t % S)) * (2 * chunks_per_row);
+        const uint4* xs = x + t * chunks_per_token;
+        uint4* ys = y + t * chunks_per_token;
+        float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0;
+        if (fixed_chunk) {
+            const int g = lane % chunks_per_row;
+            c0 = row[2 * g];
+            c1 = row[2 * g + 1];
         }
+        for (int j0 = lane; j0 < chunks_per_token; j0 += 32 * kUnroll) {
+            uint4 w[kUnroll];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-            const long long c = c0 + u * stride;
-            if (c >= n_chunks) break;
-            const long long row = c / chunks_per_row;           // (b, s, h) flattened
-            const int g = (int)(c % chunks_per_row);
-            const long long pos = pos0 + (row / H) % S;
-            const float4* cs = table + pos * (D / 4) + 2 * g;
-            const float4 t0 = cs[0], t1 = cs[1];
-            uint4 r;
-            r.x = attn::rotate_pair<BF16>(w[u].x, t0.x, t0.y);
-            r.y = attn::rotate_pair<BF16>(w[u].y, t0.z, t0.w);
-            r.z = attn::rotate_pair<BF16>(w[u].z, t1.x, t1.y);
-            r.w = attn::rotate_pair<BF16>(w[u].w, t1.z, t1.w);
-            y[c] = r;
+            for (int u = 0; u < kUnroll; ++u) {
+                const int j = j0 + 32 * u;
+                if (j < chunks_per_token) w[u] = xs[j];
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int j = j0 + 32 * u;
+                if (j >= chunks_per_token) break;
+                if (!fixed_chunk) {
+                    const int g = j % chunks_per_row;
+                    c0 = row[2 * g];
+                    c1 = row[2 * g + 1];
+                }
+                uint4 r;
+                r.x = attn::rotate_pair<BF16>(w[u].x, c0.x, c0.y);
+                r.y = attn::rotate_pair<BF16>(w[u].y, c0.z, c0.w);
+                r.z = attn::rotate_pair<BF16>(w[u].z, c1.x, c1.y);
+                r.w = attn::rotate_pair<BF16>(w[u].w, c1.z, c1.w);
+                ys[j] = r;
+            }
         }
     }
 }
@@ -289,6 +305,22 @@ unsigned elementwise_grid(long long work, int num_sms) {
     return (unsigned)std::max(1LL, std::min(blocks, 8LL * num_sms));
 }
 
+// Enqueues the key / tensor rotation pass over a (B, S, H, D) tensor.
+int launch_rope_apply(const void* x, void* y, int B, int S, int H, int D, const float* table, int pos0, bool bf16,
+                      int num_sms, cudaStream_t stream) {
+    const long long n_tokens = (long long)B * S;
+    const int per_token = H * (D / 8), per_row = D / 8;
+    const unsigned grid = (unsigned)std::max(1LL, std::min((n_tokens + 7) / 8, 8LL * num_sms));   // 8 warps a block
+    const auto* t4 = reinterpret_cast<const float4*>(table);
+    const auto* x4 = static_cast<const uint4*>(x);
+    auto* y4 = static_cast<uint4*>(y);
+    if (bf16)
+        rope_apply_kernel<true><<<grid, 256, 0, stream>>>(x4, y4, n_tokens, S, per_token, per_row, t4, pos0);
+    else
+        rope_apply_kernel<false><<<grid, 256, 0, stream>>>(x4, y4, n_tokens, S, per_token, per_row, t4, pos0);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                   int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, cudaStream_t stream,
                   bool bf16, int num_splits = 1, void* workspace = nullptr, size_t workspace_bytes = 0,
@@ -333,16 +365,8 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     }
 
     if (rope && rope->k_rot) {                               // rotate each key once
-        const long long n_chunks = (long long)B * Sk * Hkv * (D / 8);
-        const unsigned g = elementwise_grid(n_chunks, dev->num_sms);
-        const auto* table = reinterpret_cast<const float4*>(rope->table);
-        if (bf16)
-            rope_apply_kernel<true><<<g, 256, 0, stream>>>(static_cast<const uint4*>(k), static_cast<uint4*>(rope->k_rot),
-                                                           n_chunks, Sk, Hkv, D, table, rope->k_pos0);
-        else
-            rope_apply_kernel<false><<<g, 256, 0, stream>>>(static_cast<const uint4*>(k), static_cast<uint4*>(rope->k_rot),
-                                                            n_chunks, Sk, Hkv, D, table, rope->k_pos0);
-        if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+        rc = launch_rope_apply(k, rope->k_rot, B, Sk, Hkv, D, rope->table, rope->k_pos0, bf16, dev->num_sms, stream);
+        if (rc != ATTN_OK) return rc;
         k = rope->k_rot;
     }
 
@@ -485,22 +509,14 @@ namespace {
 int rope_apply_impl(const void* x, void* y, int B, int S, int H, int D, const float* table, int max_pos, int pos0,
                     cudaStream_t stream, bool bf16) {
     if (B < 0 || S < 0 || H < 0 || D <= 0 || D % 8 != 0 || max_pos < 0 || pos0 < 0) return ATTN_ERR_INVALID_ARG;
-    if ((long long)pos0 + S > max_pos) return ATTN_ERR_INVALID_ARG;
+    if ((long long)pos0 + S > max_pos || (long long)H * (D / 8) > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     const long long n_chunks = (long long)B * S * H * (D / 8);
     if (n_chunks == 0) return ATTN_OK;
     if (!x || !y || !table || !aligned(x, 16) || !aligned(y, 16) || !aligned(table, 16)) return ATTN_ERR_INVALID_ARG;
     DeviceInfo* dev = nullptr;
     int rc = device_info(&dev);
     if (rc != ATTN_OK) return rc;
-    const unsigned g = elementwise_grid(n_chunks, dev->num_sms);
-    const auto* t4 = reinterpret_cast<const float4*>(table);
-    if (bf16)
-        rope_apply_kernel<true><<<g, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<uint4*>(y), n_chunks, S, H,
-                                                       D, t4, pos0);
-    else
-        rope_apply_kernel<false><<<g, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<uint4*>(y), n_chunks, S,
-                                                        H, D, t4, pos0);
-    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+    return launch_rope_apply(x, y, B, S, H, D, table, pos0, bf16, dev->num_sms, stream);
 }
 
 }  // namespace

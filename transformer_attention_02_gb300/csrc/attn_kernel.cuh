@@ -109,7 +109,7 @@ struct TileCfg {
     static constexpr int bStall = bDrain + 1;
     static constexpr int bKVFull = bStall + 1;        // [kSlots]
     static constexpr int bKVEmpty = bKVFull + kSlots;
-    static constexpr int bQRdy = bKVEmpty + kSlots;   // [kQBufs] rotary variant: Q sub-tile rotated
+    static constexpr int bQRdy = bKVEmpty + kSlots;   // [kQBufs] rotary variant: Q rotated (two arrivals)
     static constexpr int kNumBars = bQRdy + kQBufs;
     static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
@@ -282,11 +282,18 @@ __device__ __forceinline__ uint32_t rotate_pair(uint32_t w, float c, float s) {
 
 // One warp rotates rows [r_begin, r_end) of a 128 x D sub-tile held as
 // 128-byte-swizzled 64-column boxes; the sub-tile's row r is query row
-// row0 + r. Each lane moves 16 bytes (four pairs) at a time. Rows at or past
-// Sq (zero fill of the load) are skipped. The writes are made visible to the
-// tensor core's (async) proxy before the caller signals.
+// row0 + r. Each lane owns one 16-byte chunk of the row (four pairs) and
+// visits every kRowsPerPass-th row. It reads the {cos, sin} of its four pairs
+// from the table once, at its first row, and then advances them by the fixed
+// angle of kRowsPerPass positions with the angle-addition formulas
+//   cos(a + d) = cos a cos d - sin a sin d,  sin(a + d) = sin a cos d + cos a sin d,
+// so the loop touches only shared memory (no table fetch on its critical
+// path). Over the at most 64 steps of a sub-tile the FP32 recurrence drifts by
+// a few 2^-24 per step, far below the 16-bit spacing of the results. Rows at
+// or past Sq (zero fill of the load) are skipped. The writes are made visible
+// to the tensor core's (async) proxy before the caller signals.
 template <int D, bool BF16>
-__device__ void rope_rotate_rows(uint8_t* tile, int r_begin, int r_end, int row0, const FwdParams& p) {
+__device__ __forceinline__ void rope_rotate_rows(uint8_t* tile, int r_begin, int r_end, int row0, const FwdParams& p) {
     using C = TileCfg<D>;
     constexpr int kChunks = D / 8;                 // 16-byte chunks per row
     constexpr int kRowsPerPass = 32 / kChunks;
@@ -294,18 +301,31 @@ __device__ void rope_rotate_rows(uint8_t* tile, int r_begin, int r_end, int row0
     const int g = lane % kChunks;                  // chunk of the row: pairs 4g .. 4g+3
     const int box = g / 8, k = g % 8;
     const int r_stop = min(r_end, p.Sq - row0);
-    const float4* table = reinterpret_cast<const float4*>(p.rope) + 2 * g;
-#pragma unroll 4
-    for (int r = r_begin + lane / kChunks; r < r_stop; r += kRowsPerPass) {
-        uint4* ptr = reinterpret_cast<uint4*>(tile + box * C::kBoxBytes + r * 128 + ((k ^ (r & 7)) << 4));
-        const float4* cs = table + (size_t)(p.q_pos0 + row0 + r) * (D / 4);
-        const float4 t0 = __ldg(cs), t1 = __ldg(cs + 1);      // (c, s) of pairs 4g .. 4g+3
-        uint4 w = *ptr;
-        w.x = rotate_pair<BF16>(w.x, t0.x, t0.y);
-        w.y = rotate_pair<BF16>(w.y, t0.z, t0.w);
-        w.z = rotate_pair<BF16>(w.z, t1.x, t1.y);
-        w.w = rotate_pair<BF16>(w.w, t1.z, t1.w);
-        *ptr = w;
+    int r = r_begin + lane / kChunks;
+    if (r < r_stop) {
+        const float4* table = reinterpret_cast<const float4*>(p.rope) + 2 * g;
+        const float4* at = table + (size_t)(p.q_pos0 + row0 + r) * (D / 4);
+        float4 a0 = __ldg(at), a1 = __ldg(at + 1);                       // {cos, sin} of the four pairs
+        float4 d0 = make_float4(1.f, 0.f, 1.f, 0.f), d1 = d0;
+        if (r + kRowsPerPass < r_stop) {                                 // step: position kRowsPerPass
+            d0 = __ldg(table + kRowsPerPass * (D / 4));
+            d1 = __ldg(table + kRowsPerPass * (D / 4) + 1);
+        }
+        uint8_t* col = tile + box * C::kBoxBytes;
+#pragma unroll 2
+        for (; r < r_stop; r += kRowsPerPass) {
+            uint4* ptr = reinterpret_cast<uint4*>(col + r * 128 + ((k ^ (r & 7)) << 4));
+            uint4 w = *ptr;
+            w.x = rotate_pair<BF16>(w.x, a0.x, a0.y);
+            w.y = rotate_pair<BF16>(w.y, a0.z, a0.w);
+            w.z = rotate_pair<BF16>(w.z, a1.x, a1.y);
+            w.w = rotate_pair<BF16>(w.w, a1.z, a1.w);
+            *ptr = w;
+            a0 = make_float4(a0.x * d0.x - a0.y * d0.y, a0.y * d0.x + a0.x * d0.y,
+                             a0.z * d0.z - a0.w * d0.w, a0.w * d0.z + a0.z * d0.w);
+            a1 = make_float4(a1.x * d1.x - a1.y * d1.y, a1.y * d1.x + a1.x * d1.y,
+                             a1.z * d1.z - a1.w * d1.w, a1.w * d1.z + a1.z * d1.w);
+        }
     }
     ptx::fence_proxy_async_shared();
     __syncwarp();
@@ -355,9 +375,7 @@ __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr
 // between two buffers, so it is fetched as soon as the tile before the current
 // one has finished with it; the upper sub-tile reuses one buffer and is fetched
 // while the previous tile's last products and epilogue run. In the rotary
-// variant this warp also rotates rows 0..63 of each sub-tile after it lands:
-// the lower sub-tile of tile T (loaded during tile T-1) first, then, once the
-// upper buffer is free, the upper one.
+// variant this warp also rotates rows 0..63 of each sub-tile after it lands.
 template <int D, bool CAUSAL, bool BF16, bool ROPE>
 __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t smem, uint8_t* smem_ptr,
                            const SyncCtx& sc) {
@@ -394,23 +412,30 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
             ++nq;
         }
     } else {
+        // Loads are issued as early as in the plain variant (the upper sub-tile
+        // of tile T as soon as its buffer is free, the next tile's lower one
+        // right after it); rotations follow in load order: the upper sub-tile
+        // of T as soon as it lands, then the next tile's lower one, which
+        // therefore is ready a whole tile ahead.
         int w = 0;
         TileInfo ti;
         bool have = next_work_tile<CAUSAL>(p, 0, w, ti) && load(0, ti.m0, ti);
+        bool lower_rotated = false;
         while (have) {
             const int b0 = nq & 1, b1 = 2 + nq % C::kQ1Bufs;
-            const bool b1_unused = uses[b1] == 0;       // first use: nothing to wait for
-            if (b1_unused && !load(b1, ti.m0 + kBlockM, ti)) break;
-            if (!rotate(b0, nq >> 1, ti.m0)) break;
-            if (!b1_unused && !load(b1, ti.m0 + kBlockM, ti)) break;
-            if (!rotate(b1, nq / C::kQ1Bufs, ti.m0 + kBlockM)) break;
+            if (!load(b1, ti.m0 + kBlockM, ti)) break;
             int w_next = 0;
             TileInfo tn;
-            have = next_work_tile<CAUSAL>(p, w + 1, w_next, tn);
-            if (have && !load((nq + 1) & 1, tn.m0, tn)) break;
+            const bool more = next_work_tile<CAUSAL>(p, w + 1, w_next, tn);
+            if (more && !load((nq + 1) & 1, tn.m0, tn)) break;
+            if (!lower_rotated && !rotate(b0, nq >> 1, ti.m0)) break;
+            if (!rotate(b1, nq / C::kQ1Bufs, ti.m0 + kBlockM)) break;
+            if (more && !rotate((nq + 1) & 1, (nq + 1) >> 1, tn.m0)) break;
+            lower_rotated = true;
             ++nq;
             w = w_next;
             ti = tn;
+            have = more;
         }
     }
     // Shut down: wait until every copy this warp started has landed.
