@@ -224,10 +224,11 @@ int attn_rope_apply_f16(const void *x, void *y, int B, int S, int H, int D,
  *
  * The queries are rotated inside the attention kernel, after each Q tile's
  * load lands in shared memory and before the tensor cores read it; no rotated
- * copy of Q exists. The keys are rotated once per key: on GB300 a 128 x D key
- * tile takes the tensor cores 256 cycles (D = 128) to use but over a thousand
- * warp instructions to rotate, and every query tile of the head would repeat
- * it, so rotating keys at tile load would make the kernel ALU-bound. Hence:
+ * copy of Q exists. The keys are rotated once per key: rotating a 128-key tile
+ * takes about 1,500 warp instructions, every query tile of the head would
+ * repeat it (8 to 64 times on typical shapes), and the SM's issue slots in the
+ * tensor cores' time for that tile (about 1,000 cycles per product pair at
+ * D = 128) are mostly taken by the softmax already. Hence:
  *   k_rot   device buffer of k's shape and layout (16-byte aligned) that
  *           receives rot(K) from a bandwidth-bound pass enqueued before the
  *           attention kernel (k_rot may equal k: the keys are then rotated in
