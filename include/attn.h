@@ -256,6 +256,45 @@ int attn_fwd_rope_f16(const void *q, const void *k, const void *v, void *o, floa
                       int num_splits, void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_fwd_host / attn_fwd_host_f16 — attn_fwd with Q, K, V, O, LSE and the
+ * mask in HOST memory (same shapes and layouts), for callers whose tensors
+ * live on the host. The pages have no counterpart: this is the copy pipeline
+ * around the fused operation, not a step of it.
+ * The problem is cut into units of one batch entry and a group of K/V heads
+ * (with their query heads); each unit's Q, K, V are copied into one of three
+ * device staging slots, the fused kernel runs on it, and its O and LSE are
+ * copied back, on three streams of the library, so that the copies of
+ * neighbouring units overlap the computation and each other. The additive
+ * mask of each batch entry is copied once. The work starts after everything
+ * already queued on `stream`, and `stream` continues only once the last copy
+ * back has finished: synchronise it before reading o and lse.
+ *   q, k, v, o, lse, mask  host pointers (any alignment; page-locked memory
+ *               from cudaHostAlloc or cudaHostRegister lets the copies run
+ *               asynchronously at full speed, pageable memory works but its
+ *               copies are staged by the driver and do not overlap).
+ *   workspace   device scratch of at least attn_fwd_host_workspace_bytes(...)
+ *               bytes, 256-byte aligned, owned by the caller; two calls in
+ *               flight on different streams need two workspaces.
+ * The library creates, on first use per device, three streams and a few
+ * events that it keeps until the process exits; calls from several host
+ * threads are serialised while they enqueue. Other arguments and errors as
+ * for attn_fwd / attn_fwd_f16; a missing, misaligned or too small workspace
+ * is ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                  float scale, int mask_kind, const float *mask,
+                  void *workspace, size_t workspace_bytes, attn_stream_t stream);
+int attn_fwd_host_f16(const void *q, const void *k, const void *v, void *o, float *lse,
+                      int B, int Hq, int Hkv, int Sq, int Sk, int D,
+                      float scale, int mask_kind, const float *mask,
+                      void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/* attn_fwd_host_workspace_bytes — device staging bytes attn_fwd_host needs
+ * (host only; 0 for an empty problem or invalid sizes). */
+size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int mask_kind);
+
+/*
  * attn_last_status — synchronises `stream`, then returns and clears the
  * current device's run-time status word: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT
  * if any launch since the last call gave up on a bounded wait (the kernel then

@@ -203,3 +203,39 @@ def test_rope_apply_arguments(lib, kw, code):
     a.update(kw)
     for fn in (A.attn_rope_apply, A.attn_rope_apply_f16):
         assert fn(a["x"], a["y"], a["B"], a["S"], a["H"], a["D"], a["table"], a["max_pos"], a["pos0"], None) == code
+
+
+# ------------------------------------------------------ host-buffer pipeline (host only)
+
+def test_host_pipeline_workspace_size(lib):
+    # Llama-2-7B shape: 4 entries x 2 groups of 16 heads = 8 units, three slots of
+    # Q + K + V + O (8 MiB each) + LSE (16 x 2048 FP32)
+    per_slot = 4 * (2048 * 16 * 128 * 2) + 16 * 2048 * 4
+    assert A.attn_fwd_host_workspace_bytes(4, 32, 32, 2048, 2048, 128, 1) == 3 * per_slot
+    # an additive mask adds B x Sq x Sk FP32, staged once
+    assert A.attn_fwd_host_workspace_bytes(4, 32, 32, 2048, 2048, 128, 3) == 3 * per_slot + 4 * 2048 * 2048 * 4
+    assert A.attn_fwd_host_workspace_bytes(0, 32, 32, 2048, 2048, 128, 1) == 0
+    assert A.attn_fwd_host_workspace_bytes(4, 32, 32, 2048, 2048, 96, 1) == 0
+
+
+def _call_host(ws=P, ws_bytes=1 << 34, **kw):
+    a = dict(q=P, k=P, v=P, o=P, lse=P, B=2, Hq=4, Hkv=2, Sq=64, Sk=64, D=128, scale=0.0, kind=1, mask=None)
+    a.update(kw)
+    return A.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"],
+                           a["D"], a["scale"], a["kind"], a["mask"], ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(ws=P + 64), A.ATTN_ERR_INVALID_ARG),                # not 256-byte aligned
+    (dict(ws_bytes=1024), A.ATTN_ERR_INVALID_ARG),
+    (dict(q=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(kind=2, mask=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3), A.ATTN_ERR_INVALID_ARG),
+    (dict(kind=5), A.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), A.ATTN_ERR_UNSUPPORTED),
+    (dict(B=0), A.ATTN_OK),
+    (dict(Sq=0), A.ATTN_OK),
+])
+def test_host_pipeline_arguments_are_checked_before_launch(lib, kw, code):
+    assert _call_host(**kw) == code

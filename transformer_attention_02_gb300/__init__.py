@@ -10,4 +10,5 @@ from .attn import (  # noqa: F401
     attn_debug_inject_stall, attn_fwd, attn_fwd_f16, attn_fwd_splitkv, attn_fwd_splitkv_f16, attn_last_status,
     attn_set_wait_timeout_ns, attn_splitkv_num_splits, attn_splitkv_workspace_bytes, attn_status_string,
     attention_splitkv, attn_fwd_rope, attn_fwd_rope_f16, attn_rope_table, attn_rope_apply, attn_rope_apply_f16,
-    attention_rope, rope_table, rope_apply)
+    attention_rope, rope_table, rope_apply, attn_fwd_host, attn_fwd_host_f16, attn_fwd_host_workspace_bytes,
+    attention_host)

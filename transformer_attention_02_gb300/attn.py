@@ -57,6 +57,11 @@ def lib() -> ctypes.CDLL:
     for f in (L.attn_rope_apply, L.attn_rope_apply_f16):
         f.argtypes = [P, P, I, I, I, I, P, I, I, P]
         f.restype = I
+    for f in (L.attn_fwd_host, L.attn_fwd_host_f16):
+        f.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, P, ctypes.c_size_t, P]
+        f.restype = I
+    L.attn_fwd_host_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+    L.attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
     L.attn_rope_table.argtypes = [P, I, I, ctypes.c_double, P]
     L.attn_rope_table.restype = I
     L.attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]
@@ -130,6 +135,22 @@ def attn_rope_apply(x, y, B, S, H, D, rope_table, max_pos, pos0, stream) -> int:
 
 def attn_rope_apply_f16(x, y, B, S, H, D, rope_table, max_pos, pos0, stream) -> int:
     return lib().attn_rope_apply_f16(x, y, B, S, H, D, rope_table, max_pos, pos0, stream)
+
+
+def attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, workspace, workspace_bytes,
+                  stream) -> int:
+    return lib().attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, workspace,
+                               workspace_bytes, stream)
+
+
+def attn_fwd_host_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, workspace, workspace_bytes,
+                      stream) -> int:
+    return lib().attn_fwd_host_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, mask, workspace,
+                                   workspace_bytes, stream)
+
+
+def attn_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, mask_kind) -> int:
+    return int(lib().attn_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, mask_kind))
 
 
 def attn_splitkv_num_splits(B, Hq, Sq, Sk, num_splits=0) -> int:
@@ -328,3 +349,49 @@ def attention_rope(q, k, v, table, *, q_pos0: int = 0, k_pos0: int = 0, k_rot="n
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_rope")
     return (out, lse) if k_rot is None else (out, lse, k_rot)
+
+
+def attention_host(q, k, v, *, causal: bool = False, mask=None, scale=None, out=None, lse=None, workspace=None,
+                   device=None, stream=None):
+    """attention() for (B, S, H, D) bf16/fp16 tensors in host memory (pin them
+    for full speed): copies in, computes and copies back in a pipeline on the
+    GPU. Returns (out, lse) in host memory, written once `stream` (default: the
+    current stream of `device`) has been synchronised; this function does not
+    synchronise. workspace: optional uint8 CUDA tensor of at least
+    attn_fwd_host_workspace_bytes bytes (allocated here when omitted).
+    """
+    import torch
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q, k, v must be bf16 or fp16")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not (t.device.type == "cpu" and t.dtype == q.dtype and t.dim() == 4 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous 4-D host tensor (B, S, H, D) of q's dtype")
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if (Bk, Dk) != (B, D) or v.shape != k.shape:
+        raise ValueError("q, k, v shapes disagree")
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, pin_memory=pin)
+    kind = (MASK_CAUSAL if causal else MASK_NONE) + (MASK_ADDITIVE if mask is not None else 0)
+    mptr = None
+    if mask is not None:
+        if not (mask.device.type == "cpu" and mask.dtype == torch.float32 and mask.is_contiguous()
+                and tuple(mask.shape) == (B, Sq, Sk)):
+            raise ValueError("mask must be a contiguous FP32 host tensor of shape (B, Sq, Sk)")
+        mptr = mask.data_ptr()
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    need = attn_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, kind)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    sc = float("nan") if scale is None else float(scale)
+    fn = attn_fwd_host if q.dtype == torch.bfloat16 else attn_fwd_host_f16
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Sq, Sk, D, sc,
+                kind, mptr, workspace.data_ptr(), workspace.numel() * workspace.element_size(), s.cuda_stream)
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host")
+    return out, lse
