@@ -295,6 +295,62 @@ int attn_fwd_host_f16(const void *q, const void *k, const void *v, void *o, floa
 size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int mask_kind);
 
 /*
+ * The attention block ("ATB orchestration blog"
+ * (hwcomputing.csdn.net/6a15a709662f9a54cb774da1) section 2, the fused
+ * attention block of the graph-operator layer and its GraphOp listing):
+ *     n   = LayerNorm(x)                (eps, gain gamma, bias beta; over hidden)
+ *     qkv = n W_qkv^T + b_qkv           [q | k | v] per token, (Hq + 2 Hkv) D features
+ *     a   = attention(q, k, v)          fused kernel above, scale 1/sqrt(D)
+ *     y   = a W_o^T + b_o + x           output projection and residual
+ * bf16 tensors, FP32 accumulation and statistics; the intermediate tensors n,
+ * qkv and a are bf16 in a caller workspace (each GEMM needs whole rows of its
+ * input, so they pass through device memory once). Four launches: LayerNorm,
+ * the QKV GEMM with its bias fused in the epilogue, the attention reading q,
+ * k, v straight from the packed projection output, and the output GEMM with
+ * bias and residual fused in the epilogue.
+ *
+ * attn_layernorm — y = (x - mean) / sqrt(var + eps) * gamma + beta for each of
+ * M rows of H values (biased variance; FP32 statistics). x, y (M, H) bf16;
+ * gamma, beta (H) bf16; all 16-byte aligned; H a multiple of 8, 8..8192.
+ * eps not finite or <= 0 selects 1e-5. y may equal x.
+ */
+int attn_layernorm(const void *x, const void *gamma, const void *beta, void *y, int M, int H, float eps,
+                   attn_stream_t stream);
+
+/*
+ * attn_linear — out = a w^T (+ bias) (+ residual) on the tensor cores.
+ * a (M, K), w (N, K), residual and out (M, N), bias (N): bf16, row-major,
+ * contiguous, 16-byte aligned; bias and residual may be NULL; out may equal
+ * residual. N a positive multiple of 32, K a positive multiple of 8.
+ */
+int attn_linear(const void *a, const void *w, const void *bias, const void *residual, void *out,
+                int M, int N, int K, attn_stream_t stream);
+
+/*
+ * attn_fwd_qkvpacked — attn_fwd (bf16, self-attention: Sq = Sk = S) with q, k,
+ * v taken from one packed tensor qkv (B, S, (Hq + 2 Hkv) D): the features of
+ * token (b, s) are [q heads | k heads | v heads], as a fused QKV projection
+ * writes them. o (B, S, Hq, D) and lse (B, Hq, S) as for attn_fwd.
+ */
+int attn_fwd_qkvpacked(const void *qkv, void *o, float *lse, int B, int S, int Hq, int Hkv, int D,
+                       float scale, int mask_kind, const float *mask, attn_stream_t stream);
+
+/*
+ * attn_block_fwd — the attention block on x (B, S, Hq D) bf16:
+ *   ln_gamma, ln_beta (Hq D); w_qkv ((Hq + 2 Hkv) D, Hq D), b_qkv ((Hq + 2 Hkv) D);
+ *   w_o (Hq D, Hq D), b_o (Hq D); y (B, S, Hq D) (may equal x). All bf16,
+ *   contiguous, 16-byte aligned. causal != 0 applies the causal mask.
+ *   eps as for attn_layernorm. D in {64, 128}; Hq D at most 8192.
+ *   workspace: device scratch of attn_block_workspace_bytes(...) bytes,
+ *   256-byte aligned (it receives n, qkv, the attention output and its LSE).
+ */
+int attn_block_fwd(const void *x, const void *ln_gamma, const void *ln_beta, const void *w_qkv,
+                   const void *b_qkv, const void *w_o, const void *b_o, void *y,
+                   int B, int S, int Hq, int Hkv, int D, float eps, int causal,
+                   void *workspace, size_t workspace_bytes, attn_stream_t stream);
+size_t attn_block_workspace_bytes(int B, int S, int Hq, int Hkv, int D);
+
+/*
  * attn_last_status — synchronises `stream`, then returns and clears the
  * current device's run-time status word: ATTN_OK, or ATTN_ERR_DEVICE_TIMEOUT
  * if any launch since the last call gave up on a bounded wait (the kernel then

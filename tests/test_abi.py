@@ -239,3 +239,60 @@ def _call_host(ws=P, ws_bytes=1 << 34, **kw):
 ])
 def test_host_pipeline_arguments_are_checked_before_launch(lib, kw, code):
     assert _call_host(**kw) == code
+
+
+# ------------------------------------------------------------ attention block (host only)
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=48), A.ATTN_ERR_INVALID_ARG),                    # N must be a multiple of 32
+    (dict(K=12), A.ATTN_ERR_INVALID_ARG),                    # K a multiple of 8
+    (dict(N=0), A.ATTN_ERR_INVALID_ARG),
+    (dict(M=-1), A.ATTN_ERR_INVALID_ARG),
+    (dict(a=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(w=P + 8), A.ATTN_ERR_INVALID_ARG),
+    (dict(bias=P + 2), A.ATTN_ERR_INVALID_ARG),
+    (dict(M=0), A.ATTN_OK),
+])
+def test_linear_arguments(lib, kw, code):
+    a = dict(a=P, w=P, bias=None, residual=None, out=P, M=64, N=64, K=64)
+    a.update(kw)
+    assert A.attn_linear(a["a"], a["w"], a["bias"], a["residual"], a["out"], a["M"], a["N"], a["K"], None) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=12), A.ATTN_ERR_INVALID_ARG),
+    (dict(H=8200), A.ATTN_ERR_INVALID_ARG),
+    (dict(gamma=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(y=P + 4), A.ATTN_ERR_INVALID_ARG),
+    (dict(M=0), A.ATTN_OK),
+])
+def test_layernorm_arguments(lib, kw, code):
+    a = dict(x=P, gamma=P, beta=P, y=P, M=8, H=256)
+    a.update(kw)
+    assert A.attn_layernorm(a["x"], a["gamma"], a["beta"], a["y"], a["M"], a["H"], 1e-5, None) == code
+
+
+def test_block_workspace_layout(lib):
+    # n (M x H), packed qkv (M x 3H), attention output (M x H) in bf16, then FP32 LSE
+    B, S, Hq, D = 4, 2048, 32, 128
+    M, H = B * S, Hq * D
+    assert A.attn_block_workspace_bytes(B, S, Hq, Hq, D) == (M * H + M * 3 * H + M * H) * 2 + B * Hq * S * 4
+    assert A.attn_block_workspace_bytes(B, S, Hq, 8, D) == (M * H + M * (Hq + 16) * D + M * H) * 2 + B * Hq * S * 4
+    assert A.attn_block_workspace_bytes(1, 16, 4, 4, 96) == 0          # head dimension
+    assert A.attn_block_workspace_bytes(1, 16, 128, 128, 128) == 0     # hidden above 8192
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(ws_bytes=100), A.ATTN_ERR_INVALID_ARG),
+    (dict(D=96), A.ATTN_ERR_UNSUPPORTED),
+    (dict(Hq=3, Hkv=2), A.ATTN_ERR_INVALID_ARG),
+    (dict(b_qkv=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(x=P + 8), A.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), A.ATTN_OK),
+])
+def test_block_arguments(lib, kw, code):
+    a = dict(x=P, g=P, b=P, w_qkv=P, b_qkv=P, w_o=P, b_o=P, y=P, B=1, S=64, Hq=4, Hkv=4, D=64, ws=P, ws_bytes=1 << 30)
+    a.update(kw)
+    assert A.attn_block_fwd(a["x"], a["g"], a["b"], a["w_qkv"], a["b_qkv"], a["w_o"], a["b_o"], a["y"], a["B"], a["S"],
+                            a["Hq"], a["Hkv"], a["D"], 1e-5, 1, a["ws"], a["ws_bytes"], None) == code

@@ -11,4 +11,5 @@ from .attn import (  # noqa: F401
     attn_set_wait_timeout_ns, attn_splitkv_num_splits, attn_splitkv_workspace_bytes, attn_status_string,
     attention_splitkv, attn_fwd_rope, attn_fwd_rope_f16, attn_rope_table, attn_rope_apply, attn_rope_apply_f16,
     attention_rope, rope_table, rope_apply, attn_fwd_host, attn_fwd_host_f16, attn_fwd_host_workspace_bytes,
-    attention_host)
+    attention_host, attn_linear, attn_layernorm, attn_fwd_qkvpacked, attn_block_fwd, attn_block_workspace_bytes,
+    linear, layernorm, attention_qkvpacked, attention_block)

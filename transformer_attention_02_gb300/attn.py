@@ -62,6 +62,16 @@ def lib() -> ctypes.CDLL:
         f.restype = I
     L.attn_fwd_host_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
     L.attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+    L.attn_linear.argtypes = [P, P, P, P, P, I, I, I, P]
+    L.attn_linear.restype = I
+    L.attn_layernorm.argtypes = [P, P, P, P, I, I, ctypes.c_float, P]
+    L.attn_layernorm.restype = I
+    L.attn_fwd_qkvpacked.argtypes = [P, P, P, I, I, I, I, I, ctypes.c_float, I, P, P]
+    L.attn_fwd_qkvpacked.restype = I
+    L.attn_block_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, ctypes.c_float, I, P, ctypes.c_size_t, P]
+    L.attn_block_fwd.restype = I
+    L.attn_block_workspace_bytes.argtypes = [I, I, I, I, I]
+    L.attn_block_workspace_bytes.restype = ctypes.c_size_t
     L.attn_rope_table.argtypes = [P, I, I, ctypes.c_double, P]
     L.attn_rope_table.restype = I
     L.attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]
@@ -151,6 +161,28 @@ def attn_fwd_host_f16(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, scale, mask_kind, 
 
 def attn_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, mask_kind) -> int:
     return int(lib().attn_fwd_host_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, mask_kind))
+
+
+def attn_linear(a, w, bias, residual, out, M, N, K, stream) -> int:
+    return lib().attn_linear(a, w, bias, residual, out, M, N, K, stream)
+
+
+def attn_layernorm(x, gamma, beta, y, M, H, eps, stream) -> int:
+    return lib().attn_layernorm(x, gamma, beta, y, M, H, eps, stream)
+
+
+def attn_fwd_qkvpacked(qkv, o, lse, B, S, Hq, Hkv, D, scale, mask_kind, mask, stream) -> int:
+    return lib().attn_fwd_qkvpacked(qkv, o, lse, B, S, Hq, Hkv, D, scale, mask_kind, mask, stream)
+
+
+def attn_block_fwd(x, ln_gamma, ln_beta, w_qkv, b_qkv, w_o, b_o, y, B, S, Hq, Hkv, D, eps, causal, workspace,
+                   workspace_bytes, stream) -> int:
+    return lib().attn_block_fwd(x, ln_gamma, ln_beta, w_qkv, b_qkv, w_o, b_o, y, B, S, Hq, Hkv, D, eps, causal,
+                                workspace, workspace_bytes, stream)
+
+
+def attn_block_workspace_bytes(B, S, Hq, Hkv, D) -> int:
+    return int(lib().attn_block_workspace_bytes(B, S, Hq, Hkv, D))
 
 
 def attn_splitkv_num_splits(B, Hq, Sq, Sk, num_splits=0) -> int:
@@ -395,3 +427,95 @@ def attention_host(q, k, v, *, causal: bool = False, mask=None, scale=None, out=
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_host")
     return out, lse
+
+
+def _bf16_cuda(name, t, dim=None):
+    import torch
+    if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous() and (dim is None or t.dim() == dim)):
+        raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor" + (f" with {dim} dimensions" if dim else ""))
+
+
+def linear(a, w, bias=None, residual=None, *, out=None, stream=None):
+    """out = a w^T (+ bias) (+ residual) for bf16 CUDA tensors a (M, K), w (N, K)."""
+    import torch
+    _bf16_cuda("a", a, 2)
+    _bf16_cuda("w", w, 2)
+    M, K = a.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError("a and w disagree on K")
+    for name, t, shape in (("bias", bias, (N,)), ("residual", residual, (M, N))):
+        if t is not None:
+            _bf16_cuda(name, t)
+            if tuple(t.shape) != shape:
+                raise ValueError(f"{name} must have shape {shape}")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    rc = attn_linear(a.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+                     None if residual is None else residual.data_ptr(), out.data_ptr(), M, N, K, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_linear")
+    return out
+
+
+def layernorm(x, gamma, beta, eps: float = 1e-5, *, out=None, stream=None):
+    """Row-wise LayerNorm over the last dimension of a bf16 CUDA tensor."""
+    import torch
+    for name, t in (("x", x), ("gamma", gamma), ("beta", beta)):
+        _bf16_cuda(name, t)
+    H = x.shape[-1]
+    M = x.numel() // H if H else 0
+    if out is None:
+        out = torch.empty_like(x)
+    rc = attn_layernorm(x.data_ptr(), gamma.data_ptr(), beta.data_ptr(), out.data_ptr(), M, H, float(eps),
+                        _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_layernorm")
+    return out
+
+
+def attention_qkvpacked(qkv, Hq: int, Hkv: int, D: int, *, causal: bool = False, scale=None, out=None, lse=None,
+                        stream=None):
+    """Self-attention on a packed (B, S, (Hq + 2 Hkv) D) bf16 tensor [q | k | v]."""
+    import torch
+    _bf16_cuda("qkv", qkv, 3)
+    B, S, F = qkv.shape
+    if F != (Hq + 2 * Hkv) * D:
+        raise ValueError("qkv's last dimension must be (Hq + 2 Hkv) D")
+    if out is None:
+        out = torch.empty((B, S, Hq, D), dtype=torch.bfloat16, device=qkv.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, S), dtype=torch.float32, device=qkv.device)
+    sc = float("nan") if scale is None else float(scale)
+    rc = attn_fwd_qkvpacked(qkv.data_ptr(), out.data_ptr(), lse.data_ptr(), B, S, Hq, Hkv, D, sc,
+                            MASK_CAUSAL if causal else MASK_NONE, None, _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_qkvpacked")
+    return out, lse
+
+
+def attention_block(x, ln_gamma, ln_beta, w_qkv, b_qkv, w_o, b_o, *, Hq: int, Hkv: int, D: int,
+                    causal: bool = True, eps: float = 1e-5, out=None, workspace=None, stream=None):
+    """The attention block (LayerNorm, QKV projection, attention, output
+    projection, residual) on x (B, S, Hq*D) bf16 CUDA; returns y."""
+    import torch
+    for name, t in (("x", x), ("ln_gamma", ln_gamma), ("ln_beta", ln_beta), ("w_qkv", w_qkv), ("b_qkv", b_qkv),
+                    ("w_o", w_o), ("b_o", b_o)):
+        _bf16_cuda(name, t)
+    B, S, H = x.shape
+    F = (Hq + 2 * Hkv) * D
+    if H != Hq * D or tuple(w_qkv.shape) != (F, H) or tuple(b_qkv.shape) != (F,) or tuple(w_o.shape) != (H, H) \
+            or tuple(b_o.shape) != (H,) or tuple(ln_gamma.shape) != (H,) or tuple(ln_beta.shape) != (H,):
+        raise ValueError("attention block shapes disagree")
+    if out is None:
+        out = torch.empty_like(x)
+    need = attn_block_workspace_bytes(B, S, Hq, Hkv, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    rc = attn_block_fwd(x.data_ptr(), ln_gamma.data_ptr(), ln_beta.data_ptr(), w_qkv.data_ptr(), b_qkv.data_ptr(),
+                        w_o.data_ptr(), b_o.data_ptr(), out.data_ptr(), B, S, Hq, Hkv, D, float(eps),
+                        1 if causal else 0, workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                        _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_block_fwd")
+    return out

@@ -21,6 +21,7 @@
 #include "../../include/attn.h"
 #include "attn_kernel.cuh"
 #include "attn_launch.h"
+#include "block_params.h"
 
 namespace {
 
@@ -40,6 +41,7 @@ struct DeviceInfo {
     int num_sms = 0;
     unsigned int* status = nullptr;     // device address of g_device_status
     bool smem_attr_set[2][4][2][2] = {};   // [D is 128][mask kind][bf16][rotary]
+    bool gemm_attr_set = false;
 };
 
 std::mutex g_mutex;
@@ -87,9 +89,11 @@ int device_info(DeviceInfo** out) {
 
 // 4-D map over a (B, S, H, D) 16-bit tensor, innermost first: (D, H, S, B).
 // One box = 64 head-dim columns (128 bytes, the swizzle span) x 128 rows of S.
-int encode_bshd(CUtensorMap* map, const void* base, int B, int S, int H, int D, bool bf16) {
+// token_stride: elements from one (b, s) to the next (0: H * D, contiguous).
+int encode_bshd(CUtensorMap* map, const void* base, int B, int S, int H, int D, bool bf16, long long token_stride = 0) {
+    const long long ts = token_stride > 0 ? token_stride : (long long)H * D;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)S * H * D * 2};
+    const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)ts * 2, (cuuint64_t)S * ts * 2};
     const cuuint32_t box[4] = {64, 1, 128, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
@@ -324,7 +328,7 @@ int launch_rope_apply(const void* x, void* y, int B, int S, int H, int D, const 
 int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                   int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, cudaStream_t stream,
                   bool bf16, int num_splits = 1, void* workspace = nullptr, size_t workspace_bytes = 0,
-                  const RopeArgs* rope = nullptr) {
+                  const RopeArgs* rope = nullptr, long long q_stride = 0, long long kv_stride = 0) {
     // ---- arguments (host only, nothing enqueued yet)
     if (B < 0 || Hq < 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_ADDITIVE) return ATTN_ERR_INVALID_ARG;
@@ -371,8 +375,9 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     }
 
     CUtensorMap tq, tk, tv;
-    if (encode_bshd(&tq, q, B, Sq, Hq, D, bf16) != ATTN_OK || encode_bshd(&tk, k, B, Sk, Hkv, D, bf16) != ATTN_OK ||
-        encode_bshd(&tv, v, B, Sk, Hkv, D, bf16) != ATTN_OK)
+    if (encode_bshd(&tq, q, B, Sq, Hq, D, bf16, q_stride) != ATTN_OK ||
+        encode_bshd(&tk, k, B, Sk, Hkv, D, bf16, kv_stride) != ATTN_OK ||
+        encode_bshd(&tv, v, B, Sk, Hkv, D, bf16, kv_stride) != ATTN_OK)
         return ATTN_ERR_CUDA;
 
     attn::FwdParams p{};
@@ -531,6 +536,165 @@ int attn_rope_apply(const void* x, void* y, int B, int S, int H, int D, const fl
 int attn_rope_apply_f16(const void* x, void* y, int B, int S, int H, int D, const float* rope_table, int max_pos,
                         int pos0, attn_stream_t stream) {
     return rope_apply_impl(x, y, B, S, H, D, rope_table, max_pos, pos0, reinterpret_cast<cudaStream_t>(stream), false);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------ attention block
+namespace {
+
+// 2-D map over a row-major (rows x cols) bf16 matrix: boxes of 64 columns
+// (128 bytes, the swizzle span) x box_rows rows; out-of-range reads are zero.
+int encode_rows(CUtensorMap* map, const void* base, long long rows, long long cols, int box_rows) {
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+bool linear_args_ok(const void* a, const void* w, const void* bias, const void* residual, const void* out, int M, int N,
+                    int K) {
+    if (M < 0 || N <= 0 || K <= 0 || N % 32 != 0 || K % 8 != 0) return false;
+    if ((long long)M * N > (1LL << 40) || (long long)M * K > (1LL << 40)) return false;
+    if (M == 0) return true;
+    if (!a || !w || !out) return false;
+    return aligned(a, 16) && aligned(w, 16) && aligned(out, 16) && aligned(bias, 16) && aligned(residual, 16);
+}
+
+// Enqueues out = a w^T (+ bias) (+ residual); arguments already checked.
+int linear_impl(DeviceInfo& dev, const void* a, const void* w, const void* bias, const void* residual, void* out, int M,
+                int N, int K, cudaStream_t stream) {
+    if (M == 0) return ATTN_OK;
+    CUtensorMap ta, tw;
+    if (encode_rows(&ta, a, M, K, attn::gemm::kBM) != ATTN_OK || encode_rows(&tw, w, N, K, attn::gemm::kBN) != ATTN_OK)
+        return ATTN_ERR_CUDA;
+    attn::gemm::GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.bias = static_cast<const uint16_t*>(bias);
+    p.residual = static_cast<const uint16_t*>(residual);
+    p.out = static_cast<uint16_t*>(out);
+    p.ldo = N;
+    p.ldr = N;
+    p.tiles_m = ceil_div(M, attn::gemm::kBM);
+    p.tiles_n = ceil_div(N, attn::gemm::kBN);
+    p.n_tiles = p.tiles_m * p.tiles_n;
+    p.k_steps = ceil_div(K, attn::gemm::kBK);
+    p.timeout_ns = g_timeout_ns.load();
+    p.status = dev.status;
+    const int grid = p.n_tiles < dev.num_sms ? p.n_tiles : dev.num_sms;
+    return attn::gemm::launch(dev.gemm_attr_set, ta, tw, p, grid, stream);
+}
+
+bool layernorm_args_ok(const void* x, const void* gamma, const void* beta, const void* y, int M, int H) {
+    if (M < 0 || H < 8 || H > 8192 || H % 8 != 0) return false;
+    if (M == 0) return true;
+    if (!x || !gamma || !beta || !y) return false;
+    return aligned(x, 16) && aligned(gamma, 16) && aligned(beta, 16) && aligned(y, 16);
+}
+
+float layernorm_eps(float eps) { return (eps > 0.f && std::isfinite(eps)) ? eps : 1e-5f; }
+
+// Workspace of attn_block_fwd: normalised x, packed q|k|v, attention output
+// (each bf16, 256-byte aligned), then the FP32 LSE.
+struct BlockLayout {
+    size_t n_off, qkv_off, a_off, lse_off, total;
+};
+
+bool block_layout(int B, int S, int Hq, int Hkv, int D, BlockLayout* L) {
+    if (B < 0 || S < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || (D != 64 && D != 128)) return false;
+    const long long M = (long long)B * S, hidden = (long long)Hq * D, F = (long long)(Hq + 2 * Hkv) * D;
+    if (hidden > 8192 || M > (1LL << 31)) return false;
+    auto up = [](size_t x) { return (x + kWorkspaceAlign - 1) / kWorkspaceAlign * kWorkspaceAlign; };
+    L->n_off = 0;
+    L->qkv_off = up(L->n_off + (size_t)M * hidden * 2);
+    L->a_off = up(L->qkv_off + (size_t)M * F * 2);
+    L->lse_off = up(L->a_off + (size_t)M * hidden * 2);
+    L->total = up(L->lse_off + (size_t)B * Hq * S * sizeof(float));
+    return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_linear(const void* a, const void* w, const void* bias, const void* residual, void* out, int M, int N, int K,
+                attn_stream_t stream) {
+    if (!linear_args_ok(a, w, bias, residual, out, M, N, K)) return ATTN_ERR_INVALID_ARG;
+    if (M == 0) return ATTN_OK;
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != ATTN_OK) return rc;
+    return linear_impl(*dev, a, w, bias, residual, out, M, N, K, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_layernorm(const void* x, const void* gamma, const void* beta, void* y, int M, int H, float eps,
+                   attn_stream_t stream) {
+    if (!layernorm_args_ok(x, gamma, beta, y, M, H)) return ATTN_ERR_INVALID_ARG;
+    if (M == 0) return ATTN_OK;
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != ATTN_OK) return rc;
+    return attn::launch_layernorm(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma),
+                                  static_cast<const uint16_t*>(beta), static_cast<uint16_t*>(y), M, H,
+                                  layernorm_eps(eps), dev->num_sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int Hq, int Hkv, int D, float scale,
+                       int mask_kind, const float* mask, attn_stream_t stream) {
+    if (Hkv <= 0 || Hq < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+    const long long F = (long long)(Hq + 2 * Hkv) * D;
+    const char* base = static_cast<const char*>(qkv);
+    const void* k = base ? base + (size_t)Hq * D * 2 : nullptr;
+    const void* v = base ? base + (size_t)(Hq + Hkv) * D * 2 : nullptr;
+    return attn_fwd_impl(qkv, k, v, o, lse, B, Hq, Hkv, S, S, D, scale, mask_kind, mask,
+                         reinterpret_cast<cudaStream_t>(stream), true, 1, nullptr, 0, nullptr, F, F);
+}
+
+size_t attn_block_workspace_bytes(int B, int S, int Hq, int Hkv, int D) {
+    BlockLayout L{};
+    return block_layout(B, S, Hq, Hkv, D, &L) ? L.total : 0;
+}
+
+int attn_block_fwd(const void* x, const void* ln_gamma, const void* ln_beta, const void* w_qkv, const void* b_qkv,
+                   const void* w_o, const void* b_o, void* y, int B, int S, int Hq, int Hkv, int D, float eps,
+                   int causal, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+    BlockLayout L{};
+    if (!block_layout(B, S, Hq, Hkv, D, &L)) {
+        if (B < 0 || S < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+        return ATTN_ERR_UNSUPPORTED;                       // head dimension or hidden size
+    }
+    const int M = B * S, hidden = Hq * D, F = (Hq + 2 * Hkv) * D;
+    if (M == 0) return ATTN_OK;
+    if (!workspace || !aligned(workspace, kWorkspaceAlign) || workspace_bytes < L.total) return ATTN_ERR_INVALID_ARG;
+    if (!layernorm_args_ok(x, ln_gamma, ln_beta, workspace, M, hidden)) return ATTN_ERR_INVALID_ARG;
+    if (!linear_args_ok(workspace, w_qkv, b_qkv, nullptr, workspace, M, F, hidden)) return ATTN_ERR_INVALID_ARG;
+    if (!linear_args_ok(workspace, w_o, b_o, x, y, M, hidden, hidden)) return ATTN_ERR_INVALID_ARG;
+    if (!b_qkv || !b_o) return ATTN_ERR_INVALID_ARG;
+    DeviceInfo* dev = nullptr;
+    int rc = device_info(&dev);
+    if (rc != ATTN_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    void* n = ws + L.n_off;
+    void* qkv = ws + L.qkv_off;
+    void* a = ws + L.a_off;
+    float* lse = reinterpret_cast<float*>(ws + L.lse_off);
+    rc = attn::launch_layernorm(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(ln_gamma),
+                                static_cast<const uint16_t*>(ln_beta), static_cast<uint16_t*>(n), M, hidden,
+                                layernorm_eps(eps), dev->num_sms, st);
+    if (rc != ATTN_OK) return rc;
+    rc = linear_impl(*dev, n, w_qkv, b_qkv, nullptr, qkv, M, F, hidden, st);
+    if (rc != ATTN_OK) return rc;
+    rc = attn_fwd_qkvpacked(qkv, a, lse, B, S, Hq, Hkv, D, 0.f, causal ? ATTN_MASK_CAUSAL : ATTN_MASK_NONE, nullptr,
+                            stream);
+    if (rc != ATTN_OK) return rc;
+    return linear_impl(*dev, a, w_o, b_o, x, y, M, hidden, hidden, st);
 }
 
 }  // extern "C"

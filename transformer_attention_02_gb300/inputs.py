@@ -148,3 +148,57 @@ def make_inputs(cfg: AttnConfig):
 def bits(t: torch.Tensor):
     """The raw 16-bit patterns of a bf16/fp16 CPU tensor, as a numpy uint16 array."""
     return t.contiguous().view(torch.int16).numpy().view("uint16")
+
+
+# ------------------------------------------------------------ attention block
+
+@dataclass(frozen=True)
+class BlockConfig:
+    """Sizes of one attention block: x (B, S, Hq*D) -> y (B, S, Hq*D)."""
+    name: str
+    B: int
+    S: int
+    Hq: int
+    Hkv: int
+    D: int
+    causal: bool = True
+    seed: int = 0
+
+    @property
+    def hidden(self) -> int:
+        return self.Hq * self.D
+
+    @property
+    def flops(self) -> float:
+        """Algorithmic FLOPs: the two projections (2 M N K each) plus the attention."""
+        M, H, F = self.B * self.S, self.hidden, (self.Hq + 2 * self.Hkv) * self.D
+        att = 4.0 * self.B * self.Hq * self.S * self.S * self.D
+        return 2.0 * M * F * H + 2.0 * M * H * H + (att / 2 if self.causal else att)
+
+
+BLOCK_CONFIGS = {
+    "tiny_block": BlockConfig("tiny_block", 1, 128, 2, 2, 64),
+    # one Llama-2-7B-sized layer's attention block on the prefill batch (hidden 4096, 32 heads of 128)
+    "llama2_7b_block": BlockConfig("llama2_7b_block", 4, 2048, 32, 32, 128),
+}
+
+
+def make_block_inputs(cfg: BlockConfig):
+    """x, ln_gamma, ln_beta, w_qkv, b_qkv, w_o, b_o as bf16 CPU tensors:
+    x ~ N(0, 1); gamma ~ 1 + 0.1 N(0, 1); beta, the biases ~ 0.02 N(0, 1);
+    weights ~ N(0, 1/hidden) (unit-variance projections)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(cfg.seed)
+    H, F = cfg.hidden, (cfg.Hq + 2 * cfg.Hkv) * cfg.D
+
+    def r(*shape, scale=1.0, shift=0.0):
+        return (torch.randn(shape, generator=g) * scale + shift).to(torch.bfloat16)
+
+    x = r(cfg.B, cfg.S, H)
+    gamma = r(H, scale=0.1, shift=1.0)
+    beta = r(H, scale=0.02)
+    w_qkv = r(F, H, scale=H ** -0.5)
+    b_qkv = r(F, scale=0.02)
+    w_o = r(H, H, scale=H ** -0.5)
+    b_o = r(H, scale=0.02)
+    return x, gamma, beta, w_qkv, b_qkv, w_o, b_o
