@@ -19,6 +19,11 @@ inputs resident in device memory. Prints ONE JSON line on rank 0.
 rotates the keys once (bandwidth-bound pass) and runs the attention kernel that
 rotates the queries at tile load; `value` covers both launches, `roofline` the
 attention kernel alone, and the FLOP count stays the attention's.
+`--block` runs the attention block of one Llama-2-7B-sized layer (LayerNorm,
+QKV projection, attention, output projection and residual; B=4, S=2048,
+hidden 4096) as its four kernels with CUDA events between them: `value` is the
+block's algorithmic TFLOP/s (both projections plus the causal attention),
+`roofline` the QKV projection GEMM, its dominant kernel.
 `--impl reference` times the oracle (the only reference implementation this
 method has) on the same workload and metric instead.
 Multi-GPU (torchrun): every rank runs its own replica of the workload on its
@@ -51,17 +56,22 @@ METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense bf16 tensor pe
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_SOURCES = ["transformer_attention_02_gb300/csrc/" + f for f in (
-    "attn_kernel.cuh", "ptx.cuh", "attn_api.cu", "attn_launch.h", "attn_fwd_inst.cuh", "fwd_bf16.cu",
-    "fwd_f16.cu", "fwd_rope_bf16.cu", "fwd_rope_f16.cu")]
+# Sources that decide each profiled kernel's code (the profile summaries record their hash).
+KERNEL_SOURCES = {
+    "attention": ["transformer_attention_02_gb300/csrc/" + f for f in (
+        "attn_kernel.cuh", "ptx.cuh", "attn_api.cu", "attn_launch.h", "attn_fwd_inst.cuh", "fwd_bf16.cu",
+        "fwd_f16.cu", "fwd_rope_bf16.cu", "fwd_rope_f16.cu")],
+    "gemm": ["transformer_attention_02_gb300/csrc/" + f for f in (
+        "gemm_kernel.cuh", "block_params.h", "block_kernels.cu", "attn_kernel.cuh", "ptx.cuh", "attn_api.cu")],
+}
 ROPE_BASE = 10000.0
 
 
 # ------------------------------------------------------------------ helpers
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str = "attention") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -77,17 +87,17 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources (same source hash); otherwise None."""
-    path = os.path.join(ROOT, "profiles", f"attn_fwd_{workload}.md")
+def profiled_traffic(summary: str, kernel: str = "attention"):
+    """DRAM bytes per launch from the committed ncu summary profiles/<summary>.md,
+    if it was taken on the current sources of that kernel (same hash); otherwise None."""
+    path = os.path.join(ROOT, "profiles", f"{summary}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (m_hash and m_bytes) or m_hash.group(1) != kernel_source_hash():
+    if not (m_hash and m_bytes) or m_hash.group(1) != kernel_source_hash(kernel):
         return None
     return float(m_bytes.group(1))
 
@@ -410,7 +420,7 @@ def run_ours(args, cfg):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     per_launch_s = sum(kernel_ms) / 1e3 / args.steps
     achieved = flops / per_launch_s / 1e12
-    traffic = profiled_traffic(cfg.name + ("_rope" if args.rope else ""))
+    traffic = profiled_traffic("attn_fwd_" + cfg.name + ("_rope" if args.rope else ""))
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_s / args.steps * 1e3, "higher_is_better": True,
@@ -449,6 +459,102 @@ def run_ours(args, cfg):
     return 0
 
 
+def run_block(args):
+    """The attention block, one step = LayerNorm -> QKV GEMM -> attention -> output GEMM (+ residual)."""
+    import torch.distributed as dist
+    from transformer_attention_02_gb300 import attn as A
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    A.lib()
+    cfg = I.BLOCK_CONFIGS["llama2_7b_block"]
+    host = I.make_block_inputs(cfg)
+    x, gamma, beta, w_qkv, b_qkv, w_o, b_o = (t.to(dev) for t in host)
+    M, H, F = cfg.B * cfg.S, cfg.hidden, (cfg.Hq + 2 * cfg.Hkv) * cfg.D
+    n = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+    qkv = torch.empty((cfg.B, cfg.S, F), dtype=torch.bfloat16, device=dev)
+    a = torch.empty((cfg.B, cfg.S, cfg.Hq, cfg.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((cfg.B, cfg.Hq, cfg.S), dtype=torch.float32, device=dev)
+    y = torch.empty_like(x)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    x2 = x.view(M, H)
+    stages = [
+        ("layernorm", lambda: A.layernorm(x2, gamma, beta, out=n, stream=stream)),
+        ("qkv_gemm", lambda: A.linear(n, w_qkv, b_qkv, out=qkv.view(M, F), stream=stream)),
+        ("attention", lambda: A.attention_qkvpacked(qkv, cfg.Hq, cfg.Hkv, cfg.D, causal=cfg.causal, out=a, lse=lse,
+                                                    stream=stream)),
+        ("out_gemm", lambda: A.linear(a.view(M, H), w_o, b_o, x2, out=y.view(M, H), stream=stream)),
+    ]
+    for _ in range(args.warmup):
+        flush.zero_()
+        for _, fn in stages:
+            fn()
+    torch.cuda.synchronize(dev)
+    if A.attn_last_status(stream.cuda_stream) != A.ATTN_OK:
+        raise RuntimeError("kernel reported a device timeout during warm-up")
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        for j, (_, fn) in enumerate(stages):
+            fn()
+            ev[i][j + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall1 = time.time()
+    if A.attn_last_status(stream.cuda_stream) != A.ATTN_OK:
+        raise RuntimeError("kernel reported a device timeout in the timed region")
+    per_stage = [[ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps)] for j in range(len(stages))]
+    step_ms = [ev[i][0].elapsed_time(ev[i][-1]) for i in range(args.steps)]
+    max_s = reduce_max(sum(step_ms) / 1e3, dev)
+    if rank == 0:
+        clocks.stop()
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    qkv_flops = 2.0 * M * F * H
+    qkv_ms = statistics.median(per_stage[1])
+    stage_flops = {"layernorm": 0.0, "qkv_gemm": qkv_flops, "out_gemm": 2.0 * M * H * H,
+                   "attention": cfg.flops - qkv_flops - 2.0 * M * H * H}
+    line = {
+        "metric": "attention block fwd TFLOP/s (bf16): LayerNorm + QKV GEMM + causal attention + output GEMM + "
+                  "residual", "value": whole_job_tflops(cfg.flops, args.steps, world, max_s), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_s / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "B": cfg.B, "S": cfg.S, "hidden": H, "Hq": cfg.Hq, "Hkv": cfg.Hkv,
+                   "D": cfg.D, "causal": cfg.causal, "seed": cfg.seed,
+                   "l2": "flushed before every timed step (untimed 256 MiB write)"},
+        "roofline": {"bound": "tensor", "kernel": "gemm_bf16_kernel (QKV projection, M=%d N=%d K=%d)" % (M, F, H),
+                     "achieved": qkv_flops / (qkv_ms / 1e3) / 1e12, "peak": peak, "unit": "TFLOP/s",
+                     "frac": qkv_flops / (qkv_ms / 1e3) / 1e12 / peak,
+                     "traffic": profiled_traffic("gemm_qkv_llama2_7b_block", "gemm"),
+                     "peak_source": f"{peak_src} bf16_tflops (burst)", "median_ms": qkv_ms},
+        "stages": {name: {"median_ms": statistics.median(t),
+                          "tflops": (stage_flops[name] / (statistics.median(t) / 1e3) / 1e12) if stage_flops[name]
+                          else None} for (name, _), t in zip(stages, per_stage)},
+        "gpu_launches": args.steps * len(stages),
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "kernel_source_hash": kernel_source_hash("gemm"),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -458,12 +564,16 @@ def main(argv=None):
     ap.add_argument("--config", default=I.BENCH_CONFIG, choices=sorted(I.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--block", action="store_true",
+                    help="the attention block of one Llama-2-7B-sized layer (LayerNorm, projections, attention)")
     ap.add_argument("--rope", action="store_true",
                     help="rotary position embedding: keys rotated once per step, queries inside the kernel")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     cfg = I.CONFIGS[args.config]
+    if args.block and args.impl != "reference":
+        return run_block(args)
     if args.impl == "reference":
         return run_reference(args, cfg)
     return run_ours(args, cfg)
