@@ -627,115 +627,119 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
         bool ok = true;
         const float sl = p.scale_log2;
         for (int j = 0; j < nb; ++j) {
-            // Warpgroup-uniform verdict: the named barriers below need all four warps.
-            ok = ptx::named_barrier_and(1 + wg, kBlockM, wait_phase(bar(C::bSFull + wg), s_phase, sc));
-            if (!ok) break;
+            // Each warp waits on its own; the warpgroup agrees on whether to go
+            // on at the one named barrier of the block (before the hand-off of
+            // P), where a warp whose wait ran out votes to stop.
+            const bool landed = __all_sync(0xffffffffu, wait_phase(bar(C::bSFull + wg), s_phase, sc));
             s_phase ^= 1u;
-            ptx::tc_fence_after_sync();
-            uint32_t sr[kBlockN];
+            if (landed) {
+                ptx::tc_fence_after_sync();
+                uint32_t sr[kBlockN];
 #pragma unroll
-            for (int c = 0; c < kBlockN / 32; ++c) ptx::tmem_ld32(tS + 32 * c, sr + 32 * c);
-            ptx::tmem_ld_wait();
+                for (int c = 0; c < kBlockN / 32; ++c) ptx::tmem_ld32(tS + 32 * c, sr + 32 * c);
+                ptx::tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < kBlockN / 32; ++c) ptx::reg_fence32(sr + 32 * c);
+                for (int c = 0; c < kBlockN / 32; ++c) ptx::reg_fence32(sr + 32 * c);
 
-            const int key0 = (ti.kb0 + j) * kBlockN;
-            const int vis = kv_lim - key0;                    // columns >= vis are hidden
-            // x: raw scores, or (additive mask) logits in log2 units
-            float x[kBlockN];
+                const int key0 = (ti.kb0 + j) * kBlockN;
+                const int vis = kv_lim - key0;                    // columns >= vis are hidden
+                // x: raw scores, or (additive mask) logits in log2 units
+                float x[kBlockN];
 #pragma unroll
-            for (int c = 0; c < kBlockN; ++c) x[c] = __uint_as_float(sr[c]);
-            if (ADDITIVE) {
+                for (int c = 0; c < kBlockN; ++c) x[c] = __uint_as_float(sr[c]);
+                if (ADDITIVE) {
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c) x[c] *= sl;
-                if (mrow != nullptr) {
-                    if (p.mask_vec4 && key0 + kBlockN <= p.Sk) {
-                        const float4* m4 = reinterpret_cast<const float4*>(mrow + key0);
+                    for (int c = 0; c < kBlockN; ++c) x[c] *= sl;
+                    if (mrow != nullptr) {
+                        if (p.mask_vec4 && key0 + kBlockN <= p.Sk) {
+                            const float4* m4 = reinterpret_cast<const float4*>(mrow + key0);
 #pragma unroll
-                        for (int c = 0; c < kBlockN / 4; ++c) {
-                            const float4 mv = __ldg(m4 + c);
-                            x[4 * c + 0] = fmaf(mv.x, kLog2e, x[4 * c + 0]);
-                            x[4 * c + 1] = fmaf(mv.y, kLog2e, x[4 * c + 1]);
-                            x[4 * c + 2] = fmaf(mv.z, kLog2e, x[4 * c + 2]);
-                            x[4 * c + 3] = fmaf(mv.w, kLog2e, x[4 * c + 3]);
+                            for (int c = 0; c < kBlockN / 4; ++c) {
+                                const float4 mv = __ldg(m4 + c);
+                                x[4 * c + 0] = fmaf(mv.x, kLog2e, x[4 * c + 0]);
+                                x[4 * c + 1] = fmaf(mv.y, kLog2e, x[4 * c + 1]);
+                                x[4 * c + 2] = fmaf(mv.z, kLog2e, x[4 * c + 2]);
+                                x[4 * c + 3] = fmaf(mv.w, kLog2e, x[4 * c + 3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < kBlockN; ++c)
+                                if (key0 + c < p.Sk) x[c] = fmaf(__ldg(mrow + key0 + c), kLog2e, x[c]);
                         }
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < kBlockN; ++c)
-                            if (key0 + c < p.Sk) x[c] = fmaf(__ldg(mrow + key0 + c), kLog2e, x[c]);
                     }
                 }
-            }
-            if (vis < kBlockN) {
+                if (vis < kBlockN) {
 #pragma unroll
-                for (int c = 0; c < kBlockN; ++c)
-                    if (c >= vis) x[c] = -INFINITY;
-            }
-            float mA = fmaxf(x[0], x[1]), mB = fmaxf(x[2], x[3]);
-            float mC = fmaxf(x[4], x[5]), mD = fmaxf(x[6], x[7]);
+                    for (int c = 0; c < kBlockN; ++c)
+                        if (c >= vis) x[c] = -INFINITY;
+                }
+                float mA = fmaxf(x[0], x[1]), mB = fmaxf(x[2], x[3]);
+                float mC = fmaxf(x[4], x[5]), mD = fmaxf(x[6], x[7]);
 #pragma unroll
-            for (int c = 8; c < kBlockN; c += 8) {
-                mA = ptx::max3(mA, x[c + 0], x[c + 1]);
-                mB = ptx::max3(mB, x[c + 2], x[c + 3]);
-                mC = ptx::max3(mC, x[c + 4], x[c + 5]);
-                mD = ptx::max3(mD, x[c + 6], x[c + 7]);
-            }
-            float m_blk = fmaxf(fmaxf(mA, mB), fmaxf(mC, mD));
-            if (!ADDITIVE) m_blk *= sl;                       // scale > 0 keeps the order
-            const float m_new = fmaxf(m_used, m_blk);
-            float alpha = 1.f;
-            bool rescale = false;
-            if (j == 0) {
-                m_used = m_new;
-            } else {
-                const bool need = m_new > m_used + kRescaleThreshold;
-                rescale = __any_sync(0xffffffffu, need);
-                if (need) {
-                    alpha = ptx::ex2(m_used - m_new);
-                    l_sum *= alpha;
+                for (int c = 8; c < kBlockN; c += 8) {
+                    mA = ptx::max3(mA, x[c + 0], x[c + 1]);
+                    mB = ptx::max3(mB, x[c + 2], x[c + 3]);
+                    mC = ptx::max3(mC, x[c + 4], x[c + 5]);
+                    mD = ptx::max3(mD, x[c + 6], x[c + 7]);
+                }
+                float m_blk = fmaxf(fmaxf(mA, mB), fmaxf(mC, mD));
+                if (!ADDITIVE) m_blk *= sl;                       // scale > 0 keeps the order
+                const float m_new = fmaxf(m_used, m_blk);
+                float alpha = 1.f;
+                bool rescale = false;
+                if (j == 0) {
                     m_used = m_new;
+                } else {
+                    const bool need = m_new > m_used + kRescaleThreshold;
+                    rescale = __any_sync(0xffffffffu, need);
+                    if (need) {
+                        alpha = ptx::ex2(m_used - m_new);
+                        l_sum *= alpha;
+                        m_used = m_new;
+                    }
                 }
-            }
-            if (rescale) {
-                // O_t holds the sum over the previous blocks and no product is
-                // running on it: "S_t ready" covered the previous O_t += P_t V.
+                if (rescale) {
+                    // O_t holds the sum over the previous blocks and no product is
+                    // running on it: "S_t ready" covered the previous O_t += P_t V.
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t ov[32];
-                    ptx::tmem_ld32(tO + 32 * c, ov);
-                    ptx::tmem_ld_wait();
-                    ptx::reg_fence32(ov);
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t ov[32];
+                        ptx::tmem_ld32(tO + 32 * c, ov);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence32(ov);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    ptx::tmem_st32(tO + 32 * c, ov);
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        ptx::tmem_st32(tO + 32 * c, ov);
+                    }
                 }
-            }
-            const float nm = (m_used == -INFINITY) ? 0.f : -m_used;
-            uint32_t pk[kBlockN / 2];
-            float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+                const float nm = (m_used == -INFINITY) ? 0.f : -m_used;
+                uint32_t pk[kBlockN / 2];
+                float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
 #pragma unroll
-            for (int c = 0; c < kBlockN / 2; ++c) {
-                float a, b;
-                if (ADDITIVE)
-                    ptx::add2(a, b, x[2 * c], x[2 * c + 1], nm, nm);
-                else
-                    ptx::fma2(a, b, x[2 * c], x[2 * c + 1], sl, sl, nm, nm);
-                a = ptx::ex2(a);
-                b = ptx::ex2(b);
-                if (c & 1)
-                    ptx::add2(l2, l3, l2, l3, a, b);
-                else
-                    ptx::add2(l0, l1, l0, l1, a, b);
-                pk[c] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
+                for (int c = 0; c < kBlockN / 2; ++c) {
+                    float a, b;
+                    if (ADDITIVE)
+                        ptx::add2(a, b, x[2 * c], x[2 * c + 1], nm, nm);
+                    else
+                        ptx::fma2(a, b, x[2 * c], x[2 * c + 1], sl, sl, nm, nm);
+                    a = ptx::ex2(a);
+                    b = ptx::ex2(b);
+                    if (c & 1)
+                        ptx::add2(l2, l3, l2, l3, a, b);
+                    else
+                        ptx::add2(l0, l1, l0, l1, a, b);
+                    pk[c] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
+                }
+                l_sum += (l0 + l1) + (l2 + l3);
+                ptx::tmem_st32(tS + 0, pk);
+                ptx::tmem_st32(tS + 32, pk + 32);
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before_sync();
             }
-            l_sum += (l0 + l1) + (l2 + l3);
-            ptx::tmem_st32(tS + 0, pk);
-            ptx::tmem_st32(tS + 32, pk + 32);
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before_sync();
             // All 128 rows of P_t are in TMEM once the warpgroup has met; one
             // thread then tells the MMA issuer (one arrival instead of 128).
-            ptx::named_barrier_sync(1 + wg, kBlockM);
+            ok = ptx::named_barrier_and(1 + wg, kBlockM, landed);
+            if (!ok) break;
             if (r == 0) ptx::mbar_arrive(bar(C::bPFull + wg));
         }
         if (!ok) return;
