@@ -585,6 +585,14 @@ int linear_impl(DeviceInfo& dev, const void* a, const void* w, const void* bias,
     p.tiles_n = ceil_div(N, attn::gemm::kBN);
     p.n_tiles = p.tiles_m * p.tiles_n;
     p.k_steps = ceil_div(K, attn::gemm::kBK);
+    // Raster order for L2 reuse (129 MB on GB300): when W fits in about a third
+    // of L2 it stays resident whatever the order, so small groups stream each
+    // A row panel once; otherwise a group's A row panels (about 32 MiB) stay
+    // resident while the W column panels stream past them.
+    const double w_bytes = 2.0 * N * K, a_panel = 2.0 * attn::gemm::kBM * K;
+    int group = 8;
+    if (w_bytes > 40e6) group = std::max(8, (int)((32 << 20) / a_panel));
+    p.group_rows = std::max(1, std::min(group, p.tiles_m));
     p.timeout_ns = g_timeout_ns.load();
     p.status = dev.status;
     const int grid = p.n_tiles < dev.num_sms ? p.n_tiles : dev.num_sms;

@@ -13,7 +13,6 @@ namespace gemm {
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr int kStages = 4;
 constexpr int kThreads = 192;
-constexpr int kGroupRows = 8;                                   // tile rows walked together
 constexpr int kATileBytes = kBM * kBK * 2;                      // 16 KiB
 constexpr int kBTileBytes = kBN * kBK * 2;                      // 32 KiB
 constexpr int kStageBytes = kATileBytes + kBTileBytes;
@@ -34,6 +33,7 @@ struct GemmParams {
     uint16_t* out;                // [M, ldo]
     int ldo, ldr;
     int tiles_m, tiles_n, n_tiles, k_steps;
+    int group_rows;               // tile rows walked together (L2 reuse of the W column panels)
     unsigned long long timeout_ns;
     unsigned int* status;
 };

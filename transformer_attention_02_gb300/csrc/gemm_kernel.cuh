@@ -5,8 +5,8 @@
 // Linear steps; the bias and the residual add are fused into the epilogue).
 //
 // Persistent kernel, one CTA of 192 threads per SM, tiles of 128 x 256
-// outputs walked in a grouped order (8 tile rows at a time, so that one wave
-// of CTAs shares its A rows and W columns in L2):
+// outputs walked in a grouped order (a group of tile rows at a time, column by
+// column, so that a wave of CTAs shares its A rows and W columns in L2):
 //   warp 0     TMA producer: 64-wide K slices of A (128 x 64) and W (256 x 64)
 //              into a ring of kStages 48 KiB stages (128-byte swizzle);
 //   warp 1     MMA issuer: four tcgen05.mma (M=128, N=256, K=16) per stage
@@ -25,12 +25,13 @@
 namespace attn {
 namespace gemm {
 
-// Tile t of the grouped order -> (tile row, tile column).
+// Tile t of the grouped order -> (tile row, tile column): groups of
+// group_rows tile rows, each walked column by column.
 __device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& tm, int& tn) {
-    const int per_group = kGroupRows * p.tiles_n;
+    const int per_group = p.group_rows * p.tiles_n;
     const int group = t / per_group;
-    const int first = group * kGroupRows;
-    const int rows = min(kGroupRows, p.tiles_m - first);
+    const int first = group * p.group_rows;
+    const int rows = min(p.group_rows, p.tiles_m - first);
     const int r = t - group * per_group;
     tm = first + r % rows;
     tn = r / rows;
