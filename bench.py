@@ -24,6 +24,9 @@ QKV projection, attention, output projection and residual; B=4, S=2048,
 hidden 4096) as its four kernels with CUDA events between them: `value` is the
 block's algorithmic TFLOP/s (both projections plus the causal attention),
 `roofline` the QKV projection GEMM, its dominant kernel.
+`--decode [--decode-config NAME]` times the split-key path on a decode workload
+(one new query row per sequence over a KV cache): `value` is the algorithmic
+bytes (Q, K, V read once, O and LSE written once) per second, the roofline HBM.
 `--impl reference` times the oracle (the only reference implementation this
 method has) on the same workload and metric instead.
 Multi-GPU (torchrun): every rank runs its own replica of the workload on its
@@ -60,7 +63,7 @@ L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = {
     "attention": ["transformer_attention_02_gb300/csrc/" + f for f in (
         "attn_kernel.cuh", "ptx.cuh", "attn_api.cu", "attn_launch.h", "attn_fwd_inst.cuh", "fwd_bf16.cu",
-        "fwd_f16.cu", "fwd_rope_bf16.cu", "fwd_rope_f16.cu")],
+        "fwd_f16.cu", "fwd_rope_bf16.cu", "fwd_rope_f16.cu", "fwd_pack_bf16.cu", "fwd_pack_f16.cu")],
     "gemm": ["transformer_attention_02_gb300/csrc/" + f for f in (
         "gemm_kernel.cuh", "block_params.h", "block_kernels.cu", "attn_kernel.cuh", "ptx.cuh", "attn_api.cu")],
 }
@@ -555,6 +558,86 @@ def run_block(args):
     return 0
 
 
+def run_decode(args):
+    """Decode over a KV cache through the split-key entry point (attention + merge)."""
+    from transformer_attention_02_gb300 import attn as A
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    A.lib()
+    cfg = I.DECODE_CONFIGS[args.decode_config]
+    q, k, v, _ = I.make_inputs(cfg)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(qd)
+    lse = torch.empty((cfg.B, cfg.Hq, cfg.Sq), dtype=torch.float32, device=dev)
+    splits = A.attn_splitkv_num_splits(cfg.B, cfg.Hq, cfg.Hkv, cfg.Sq, cfg.Sk, 0)
+    ws = torch.empty(max(1, A.attn_splitkv_workspace_bytes(cfg.B, cfg.Hq, cfg.Hkv, cfg.Sq, cfg.Sk, cfg.D, 0)),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def launch():
+        A.attention_splitkv(qd, kd, vd, causal=cfg.causal, num_splits=0, workspace=ws, out=o, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall1 = time.time()
+    if A.attn_last_status(stream.cuda_stream) != A.ATTN_OK:
+        raise RuntimeError("kernel reported a device timeout in the timed region")
+    ms = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+    max_s = reduce_max(sum(ms) / 1e3, dev)
+    if rank == 0:
+        clocks.stop()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    nbytes = 2 * (q.numel() + k.numel() + v.numel() + o.numel()) + 4 * lse.numel()
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = nbytes * args.steps * world / max_s / 1e9
+    med = statistics.median(ms)
+    line = {
+        "metric": "decode attention over a KV cache, GB/s of algorithmic bytes (split-key path)", "value": gbs,
+        "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": max_s / args.steps * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {**config_json(cfg), "num_splits": splits},
+        "roofline": {"bound": "hbm", "achieved": nbytes / (med / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": nbytes / (med / 1e3) / 1e9 / hbm, "traffic": None,
+                     "peak_source": f"{peak_src} hbm_gbs", "kernel": "attn_fwd_kernel + splitkv_combine_kernel",
+                     "median_ms": med},
+        "gpu_launches": args.steps * (2 if splits > 1 else 1),
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "kernel_source_hash": kernel_source_hash(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -564,6 +647,8 @@ def main(argv=None):
     ap.add_argument("--config", default=I.BENCH_CONFIG, choices=sorted(I.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode", action="store_true", help="decode over a KV cache (split-key path)")
+    ap.add_argument("--decode-config", default="gqa_decode", choices=sorted(I.DECODE_CONFIGS))
     ap.add_argument("--block", action="store_true",
                     help="the attention block of one Llama-2-7B-sized layer (LayerNorm, projections, attention)")
     ap.add_argument("--rope", action="store_true",
@@ -574,6 +659,8 @@ def main(argv=None):
     cfg = I.CONFIGS[args.config]
     if args.block and args.impl != "reference":
         return run_block(args)
+    if args.decode and args.impl != "reference":
+        return run_decode(args)
     if args.impl == "reference":
         return run_reference(args, cfg)
     return run_ours(args, cfg)

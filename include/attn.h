@@ -114,6 +114,12 @@ int attn_fwd_f16(const void *q, const void *k, const void *v, void *o, float *ls
                  float scale, int mask_kind, const float *mask, attn_stream_t stream);
 
 /*
+ * GQA head packing (all entry points except attn_fwd_rope): when the query
+ * heads per K/V head, G = Hq / Hkv, is a power of two and Sq * G <= 256 (decode
+ * and short prefills), the G query heads of a K/V head share each work tile's
+ * 128 rows, so each K/V block is streamed once per K/V head rather than once
+ * per query head. The results are those of the unpacked computation.
+ *
  * Split-key ("split-KV") variants, for few query rows against a long key/value
  * sequence: decode and short prefill over a KV cache ("ATB orchestration blog"
  * (hwcomputing.csdn.net/6a15a709662f9a54cb774da1) §四, FlashAttention with
@@ -149,13 +155,14 @@ int attn_fwd_splitkv_f16(const void *q, const void *k, const void *v, void *o, f
                          void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /* attn_splitkv_num_splits — the number of key ranges attn_fwd_splitkv uses
- * for these sizes on the current device (host only; 0 on invalid sizes). */
-int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk, int num_splits);
+ * for these sizes on the current device (host only; 0 on invalid sizes).
+ * For attn_fwd_rope pass Hkv = Hq (its tiles never pack query heads). */
+int attn_splitkv_num_splits(int B, int Hq, int Hkv, int Sq, int Sk, int num_splits);
 
 /* attn_splitkv_workspace_bytes — workspace bytes attn_fwd_splitkv needs for
  * these sizes on the current device (host only; 0 when nothing is split or
- * the sizes are invalid). */
-size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int Sk, int D, int num_splits);
+ * the sizes are invalid). For attn_fwd_rope pass Hkv = Hq. */
+size_t attn_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int num_splits);
 
 /*
  * attn_fwd_splitkv_noalloc — attn_fwd_splitkv (bf16) for callers that cannot
@@ -168,7 +175,7 @@ size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int Sk, int D, int nu
  * The pages have no counterpart; this entry point exists only for such callers.
  *
  *   Arguments, layout, results and errors as for attn_fwd_splitkv.
- *   Limit: attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits) must not
+ *   Limit: attn_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, num_splits) must not
  *   exceed 32 MiB (33554432 bytes); larger problems are refused with
  *   ATTN_ERR_UNSUPPORTED before anything is launched.
  *   The first call on each device looks up the array's device address on that

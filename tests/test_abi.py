@@ -103,22 +103,31 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
 
 def test_splitkv_range_count_and_workspace_size(lib):
     # automatic choice without a GPU (148 SMs assumed): fill one wave of tiles
-    assert A.attn_splitkv_num_splits(1, 16, 1, 8192, 0) == 8      # 16 tiles: 9 wanted, 64 blocks -> 8 x 8
-    assert A.attn_splitkv_num_splits(4, 32, 1, 4096, 0) == 1      # 128 tiles already: no split
+    assert A.attn_splitkv_num_splits(1, 16, 16, 1, 8192, 0) == 8      # 16 tiles: 9 wanted, 64 blocks -> 8 x 8
+    assert A.attn_splitkv_num_splits(4, 32, 32, 1, 4096, 0) == 1      # 128 tiles already: no split
+    # GQA decode packs the 4 query heads of each K/V head into one tile: 4 x 8 = 32
+    # tiles, so 4 ranges fill the SMs (148 // 32 = 4) instead of none
+    assert A.attn_splitkv_num_splits(4, 32, 8, 1, 4096, 0) == 4
+    # no packing for a group that is not a power of two, or too many query rows
+    assert A.attn_splitkv_num_splits(1, 32, 8, 1, 4096, 0) == 16     # 8 packed tiles: 18 wanted -> 16 x 2 blocks
+    assert A.attn_splitkv_num_splits(1, 32, 32, 1, 4096, 0) == 4     # MHA: 32 tiles -> 4 ranges
+    assert A.attn_splitkv_num_splits(4, 24, 8, 1, 4096, 0) == 1      # group of 3: 96 unpacked tiles
+    assert A.attn_splitkv_num_splits(1, 32, 8, 100, 4096, 0) == 4    # 100 x 4 rows > 256: unpacked, 32 tiles
     # explicit counts are capped by the number of 128-key blocks and made even-sized
-    assert A.attn_splitkv_num_splits(1, 8, 1, 1000, 3) == 3       # 8 blocks -> 3+3+2
-    assert A.attn_splitkv_num_splits(1, 8, 1, 1000, 100) == 8
-    assert A.attn_splitkv_num_splits(1, 8, 1, 1000, 5) == 4       # 2 blocks per range
-    assert A.attn_splitkv_num_splits(1, 8, 1, 0, 4) == 1          # no keys, no split
+    assert A.attn_splitkv_num_splits(1, 8, 8, 1, 1000, 3) == 3       # 8 blocks -> 3+3+2
+    assert A.attn_splitkv_num_splits(1, 8, 8, 1, 1000, 100) == 8
+    assert A.attn_splitkv_num_splits(1, 8, 8, 1, 1000, 5) == 4       # 2 blocks per range
+    assert A.attn_splitkv_num_splits(1, 8, 8, 1, 0, 4) == 1          # no keys, no split
     # a prefill with plenty of tiles is not split and needs no workspace
-    assert A.attn_splitkv_num_splits(4, 32, 2048, 2048, 0) == 1
-    assert A.attn_splitkv_workspace_bytes(4, 32, 2048, 2048, 128, 0) == 0
+    assert A.attn_splitkv_num_splits(4, 32, 32, 2048, 2048, 0) == 1
+    assert A.attn_splitkv_workspace_bytes(4, 32, 32, 2048, 2048, 128, 0) == 0
     # workspace = FP32 O of every range, then (256-byte aligned) FP32 LSE of every range
     rows = 4 * 32 * 1
     o_bytes = 2 * rows * 128 * 4
-    assert A.attn_splitkv_workspace_bytes(4, 32, 1, 4096, 128, 2) == ((o_bytes + 255) // 256) * 256 + 2 * rows * 4
-    assert A.attn_splitkv_workspace_bytes(4, 32, 1, 4096, 96, 2) == 0   # unsupported head dim
-    assert A.attn_splitkv_num_splits(-1, 32, 1, 4096, 0) == 0
+    assert A.attn_splitkv_workspace_bytes(4, 32, 32, 1, 4096, 128, 2) == ((o_bytes + 255) // 256) * 256 + 2 * rows * 4
+    assert A.attn_splitkv_workspace_bytes(4, 32, 32, 1, 4096, 96, 2) == 0   # unsupported head dim
+    assert A.attn_splitkv_num_splits(-1, 32, 32, 1, 4096, 0) == 0
+    assert A.attn_splitkv_num_splits(1, 32, 0, 1, 4096, 0) == 0
 
 
 def _call_split(num_splits=4, ws=P, ws_bytes=1 << 30, **kw):

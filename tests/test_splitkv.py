@@ -34,7 +34,7 @@ def test_splitkv_matches_oracle(case, dtype):
     o, lse = A.attention_splitkv(q.to(dev), k.to(dev), v.to(dev), causal=cfg.causal,
                                  mask=None if mask is None else mask.to(dev), num_splits=ns)
     torch.cuda.synchronize()
-    assert A.attn_splitkv_num_splits(B, Hq, Sq, Sk, ns) > 1
+    assert A.attn_splitkv_num_splits(B, Hq, Hkv, Sq, Sk, ns) > 1
     check(o, lse, q, k, v, mask, cfg.mask_kind, label=f"split {case} {dtype}")
 
 
@@ -54,7 +54,7 @@ def test_splitkv_with_caller_workspace_allocates_nothing():
     q, k, v, _ = I.make_inputs(cfg)
     dev = torch.device("cuda")
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    need = A.attn_splitkv_workspace_bytes(4, 32, 1, 4096, 128, 0)
+    need = A.attn_splitkv_workspace_bytes(4, 32, 8, 1, 4096, 128, 0)
     ws = torch.empty(need, dtype=torch.uint8, device=dev)
     o = torch.empty_like(qd)
     lse = torch.empty((4, 32, 1), device=dev)

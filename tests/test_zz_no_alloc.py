@@ -34,7 +34,7 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls_in_a_row():
         (I.AttnConfig("b", 1, 8, 2, 96, 3000, 128, causal=True, seed=22), 5),       # short prefill, ragged
     ]
     for cfg, ns in problems:
-        assert A.attn_splitkv_num_splits(cfg.B, cfg.Hq, cfg.Sq, cfg.Sk, ns) > 1
+        assert A.attn_splitkv_num_splits(cfg.B, cfg.Hq, cfg.Hkv, cfg.Sq, cfg.Sk, ns) > 1
         q, k, v, _ = I.make_inputs(cfg)
         qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
         ref_o, ref_l = A.attention_splitkv(qd, kd, vd, causal=cfg.causal, num_splits=ns)
@@ -66,7 +66,7 @@ def test_noalloc_allocates_nothing_per_call():
 
 def test_noalloc_refuses_a_problem_beyond_its_scratch():
     cfg = I.AttnConfig("d", 4, 32, 32, 2048, 2048, 128, causal=True)   # 4 ranges need 128+ MiB
-    assert A.attn_splitkv_workspace_bytes(cfg.B, cfg.Hq, cfg.Sq, cfg.Sk, cfg.D, 4) > 32 << 20
+    assert A.attn_splitkv_workspace_bytes(cfg.B, cfg.Hq, cfg.Hkv, cfg.Sq, cfg.Sk, cfg.D, 4) > 32 << 20
     dev = torch.device("cuda")
     qd = torch.zeros((cfg.B, cfg.Sq, cfg.Hq, cfg.D), dtype=torch.bfloat16, device=dev)
     o = torch.full_like(qd, 7.0)

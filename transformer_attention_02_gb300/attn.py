@@ -76,9 +76,9 @@ def lib() -> ctypes.CDLL:
     L.attn_rope_table.restype = I
     L.attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, ctypes.c_float, I, P, I, P]
     L.attn_fwd_splitkv_noalloc.restype = I
-    L.attn_splitkv_num_splits.argtypes = [I, I, I, I, I]
+    L.attn_splitkv_num_splits.argtypes = [I, I, I, I, I, I]
     L.attn_splitkv_num_splits.restype = I
-    L.attn_splitkv_workspace_bytes.argtypes = [I, I, I, I, I, I]
+    L.attn_splitkv_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
     L.attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
     L.attn_last_status.argtypes = [P]
     L.attn_last_status.restype = I
@@ -185,12 +185,12 @@ def attn_block_workspace_bytes(B, S, Hq, Hkv, D) -> int:
     return int(lib().attn_block_workspace_bytes(B, S, Hq, Hkv, D))
 
 
-def attn_splitkv_num_splits(B, Hq, Sq, Sk, num_splits=0) -> int:
-    return lib().attn_splitkv_num_splits(B, Hq, Sq, Sk, num_splits)
+def attn_splitkv_num_splits(B, Hq, Hkv, Sq, Sk, num_splits=0) -> int:
+    return lib().attn_splitkv_num_splits(B, Hq, Hkv, Sq, Sk, num_splits)
 
 
-def attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits=0) -> int:
-    return int(lib().attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits))
+def attn_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, num_splits=0) -> int:
+    return int(lib().attn_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, num_splits))
 
 
 def attn_last_status(stream) -> int:
@@ -280,7 +280,7 @@ def attention_splitkv(q, k, v, *, causal: bool = False, mask=None, scale=None, n
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
-    need = attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits)
+    need = attn_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, num_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     kind = (MASK_CAUSAL if causal else MASK_NONE) + (MASK_ADDITIVE if mask is not None else 0)
@@ -361,7 +361,7 @@ def attention_rope(q, k, v, table, *, q_pos0: int = 0, k_pos0: int = 0, k_rot="n
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
-    need = attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits)
+    need = attn_splitkv_workspace_bytes(B, Hq, Hq, Sq, Sk, D, num_splits)    # rotary tiles never pack heads
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     kind = (MASK_CAUSAL if causal else MASK_NONE) + (MASK_ADDITIVE if mask is not None else 0)

@@ -1,7 +1,7 @@
 """Build the CUDA library ``libattn.so`` in-tree with nvcc for sm_103a.
 
-Seven translation units (the host ABI, the host-buffer pipeline, the attention
-block's GEMM and LayerNorm, and four families of attention-kernel variants),
+Nine translation units (the host ABI, the host-buffer pipeline, the attention
+block's GEMM and LayerNorm, and six families of attention-kernel variants),
 compiled in parallel to objects under ``_build/`` and linked into one shared
 library; one -gencode, no cmake. The results sit next to this file and are
 git-ignored.
@@ -20,7 +20,7 @@ LIBRARY = os.path.join(HERE, "libattn.so")
 OBJDIR = os.path.join(HERE, "_build")
 SOURCES = [os.path.join(CSRC, f) for f in
            ("attn_api.cu", "attn_host.cu", "block_kernels.cu", "fwd_bf16.cu", "fwd_f16.cu", "fwd_rope_bf16.cu",
-            "fwd_rope_f16.cu")]
+            "fwd_rope_f16.cu", "fwd_pack_bf16.cu", "fwd_pack_f16.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in
                      ("attn_kernel.cuh", "ptx.cuh", "attn_launch.h", "attn_fwd_inst.cuh", "block_params.h",
                       "gemm_kernel.cuh")] + [

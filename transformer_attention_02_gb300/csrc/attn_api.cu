@@ -25,7 +25,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 4;
+constexpr int kAbiVersion = 5;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
 constexpr int kMaxDevices = 64;
 
@@ -40,7 +40,7 @@ struct DeviceInfo {
     bool supported = false;
     int num_sms = 0;
     unsigned int* status = nullptr;     // device address of g_device_status
-    bool smem_attr_set[2][4][2][2] = {};   // [D is 128][mask kind][bf16][rotary]
+    bool smem_attr_set[2][4][2][3] = {};   // [D is 128][mask kind][bf16][plain, rotary, packed]
     bool gemm_attr_set = false;
 };
 
@@ -90,11 +90,14 @@ int device_info(DeviceInfo** out) {
 // 4-D map over a (B, S, H, D) 16-bit tensor, innermost first: (D, H, S, B).
 // One box = 64 head-dim columns (128 bytes, the swizzle span) x 128 rows of S.
 // token_stride: elements from one (b, s) to the next (0: H * D, contiguous).
-int encode_bshd(CUtensorMap* map, const void* base, int B, int S, int H, int D, bool bf16, long long token_stride = 0) {
+// box_heads x box_rows = 128: one box is a whole 128-row sub-tile, heads
+// fastest (box_heads > 1 packs the query heads of a K/V group, see tile_info).
+int encode_bshd(CUtensorMap* map, const void* base, int B, int S, int H, int D, bool bf16, long long token_stride = 0,
+                int box_heads = 1) {
     const long long ts = token_stride > 0 ? token_stride : (long long)H * D;
     const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
     const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)ts * 2, (cuuint64_t)S * ts * 2};
-    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t box[4] = {64, (cuuint32_t)box_heads, (cuuint32_t)(128 / box_heads), 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                           const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -157,23 +160,26 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
     if (lane == 0) lse[row] = total > 0.f ? m + logf(total) : -INFINITY;
 }
 
-template <int D, bool BF16, bool ROPE>
+template <int D, bool BF16, bool ROPE, bool PACK>
 int launch_d(DeviceInfo& dev, int mask_kind, const CUtensorMap& tq, const CUtensorMap& tk,
              const CUtensorMap& tv, const attn::FwdParams& p, int grid, cudaStream_t stream) {
-    bool* attr = dev.smem_attr_set[D == 128][mask_kind][BF16 ? 1 : 0] + (ROPE ? 1 : 0);
+    bool* attr = dev.smem_attr_set[D == 128][mask_kind][BF16 ? 1 : 0] + (ROPE ? 1 : PACK ? 2 : 0);
     switch (mask_kind) {
-        case ATTN_MASK_NONE: return attn::launch_fwd<D, false, false, BF16, ROPE>(*attr, tq, tk, tv, p, grid, stream);
-        case ATTN_MASK_CAUSAL: return attn::launch_fwd<D, true, false, BF16, ROPE>(*attr, tq, tk, tv, p, grid, stream);
-        case ATTN_MASK_ADDITIVE: return attn::launch_fwd<D, false, true, BF16, ROPE>(*attr, tq, tk, tv, p, grid, stream);
-        default: return attn::launch_fwd<D, true, true, BF16, ROPE>(*attr, tq, tk, tv, p, grid, stream);
+        case ATTN_MASK_NONE:
+            return attn::launch_fwd<D, false, false, BF16, ROPE, PACK>(*attr, tq, tk, tv, p, grid, stream);
+        case ATTN_MASK_CAUSAL:
+            return attn::launch_fwd<D, true, false, BF16, ROPE, PACK>(*attr, tq, tk, tv, p, grid, stream);
+        case ATTN_MASK_ADDITIVE:
+            return attn::launch_fwd<D, false, true, BF16, ROPE, PACK>(*attr, tq, tk, tv, p, grid, stream);
+        default: return attn::launch_fwd<D, true, true, BF16, ROPE, PACK>(*attr, tq, tk, tv, p, grid, stream);
     }
 }
 
-template <bool BF16, bool ROPE>
+template <bool BF16, bool ROPE, bool PACK>
 int launch_any(DeviceInfo& dev, int D, int mask_kind, const CUtensorMap& tq, const CUtensorMap& tk,
                const CUtensorMap& tv, const attn::FwdParams& p, int grid, cudaStream_t stream) {
-    return D == 128 ? launch_d<128, BF16, ROPE>(dev, mask_kind, tq, tk, tv, p, grid, stream)
-                    : launch_d<64, BF16, ROPE>(dev, mask_kind, tq, tk, tv, p, grid, stream);
+    return D == 128 ? launch_d<128, BF16, ROPE, PACK>(dev, mask_kind, tq, tk, tv, p, grid, stream)
+                    : launch_d<64, BF16, ROPE, PACK>(dev, mask_kind, tq, tk, tv, p, grid, stream);
 }
 
 // ------------------------------------------------ rotary position embedding
@@ -261,15 +267,31 @@ int current_sm_count() {
     return sms;
 }
 
+// Head packing (see tile_info): the query heads of a K/V group share each
+// tile's rows when the group is a power of two and the whole query sequence
+// of the group fits in one tile (decode, short prefills), except with the
+// rotary embedding, whose in-kernel rotation assumes one head per tile.
+// Returns log2 of the packed heads, or 0.
+int pack_shift_for(int Hq, int Hkv, int Sq, bool rope) {
+    if (rope || Hkv <= 0 || Hq % Hkv != 0) return 0;
+    const int g = Hq / Hkv;
+    if (g < 2 || (g & (g - 1)) != 0 || g > 128 || (long long)Sq * g > attn::kRowsPerTile) return 0;
+    int s = 0;
+    while ((1 << s) < g) ++s;
+    return s;
+}
+
 // Number of key ranges for a split computation: the requested count, or (0)
 // as many as fill one wave of work tiles on the device's SMs without
 // exceeding it (1 when the unsplit tiles already cover every SM); never more
 // than there are 128-key blocks, and every range holds the same number of
 // blocks (the last may be short).
-int resolve_splits(int B, int Hq, int Sq, int Sk, int num_splits, int* split_blocks) {
+int resolve_splits(int B, int Hq, int Hkv, int Sq, int Sk, int num_splits, bool rope, int* split_blocks) {
     const int n_kb = ceil_div(Sk, attn::kBlockN);
     if (n_kb == 0) { *split_blocks = 1; return 1; }
-    const long long base_tiles = std::max(1LL, (long long)B * Hq * ceil_div(Sq, attn::kRowsPerTile));
+    const int ps = pack_shift_for(Hq, Hkv, Sq, rope);
+    const long long heads = ps ? Hkv : Hq;
+    const long long base_tiles = std::max(1LL, (long long)B * heads * ceil_div(Sq, attn::kRowsPerTile >> ps));
     int want = num_splits;
     if (want == 0) want = num_splits == 0 && base_tiles < current_sm_count() ? (int)(current_sm_count() / base_tiles) : 1;
     want = std::min(std::min(want, n_kb), kMaxSplits);
@@ -345,11 +367,14 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     if (additive && !aligned(mask, 4)) return ATTN_ERR_INVALID_ARG;
     if (Sq > (1 << 30) || Sk > (1 << 30)) return ATTN_ERR_INVALID_ARG;
     if (rope && !rope_args_ok(*rope, Sq, Sk)) return ATTN_ERR_INVALID_ARG;
-    const long long n_mblk = ((long long)Sq + attn::kRowsPerTile - 1) / attn::kRowsPerTile;
+    const int pack_shift = pack_shift_for(Hq, Hkv, Sq, rope != nullptr);
+    const long long tile_heads = pack_shift ? Hkv : Hq;
+    const long long rows_per_tile = attn::kRowsPerTile >> pack_shift;
+    const long long n_mblk = ((long long)Sq + rows_per_tile - 1) / rows_per_tile;
     if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
     int split_blocks = 1;
-    const int splits = resolve_splits(B, Hq, Sq, Sk, num_splits, &split_blocks);
-    if ((long long)B * Hq * n_mblk * splits > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    const int splits = resolve_splits(B, Hq, Hkv, Sq, Sk, num_splits, rope != nullptr, &split_blocks);
+    if ((long long)B * tile_heads * n_mblk * splits > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
     if (B == 0 || Hq == 0 || Sq == 0) return ATTN_OK;        // nothing to compute
     size_t lse_off = 0;
     if (splits > 1) {
@@ -375,7 +400,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     }
 
     CUtensorMap tq, tk, tv;
-    if (encode_bshd(&tq, q, B, Sq, Hq, D, bf16, q_stride) != ATTN_OK ||
+    if (encode_bshd(&tq, q, B, Sq, Hq, D, bf16, q_stride, 1 << pack_shift) != ATTN_OK ||
         encode_bshd(&tk, k, B, Sk, Hkv, D, bf16, kv_stride) != ATTN_OK ||
         encode_bshd(&tv, v, B, Sk, Hkv, D, bf16, kv_stride) != ATTN_OK)
         return ATTN_ERR_CUDA;
@@ -393,7 +418,8 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     p.n_mblk = (int)n_mblk;
     p.n_splits = splits;
     p.split_blocks = splits > 1 ? split_blocks : ceil_div(Sk, attn::kBlockN);
-    p.n_tiles = (int)((long long)B * Hq * n_mblk * splits);
+    p.n_tiles = (int)(B * tile_heads * n_mblk * splits);
+    p.pack_shift = pack_shift;
     if (splits > 1) {
         p.o_part = static_cast<float*>(workspace);
         p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + lse_off);
@@ -409,11 +435,14 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
 
     const int grid = p.n_tiles < dev->num_sms ? p.n_tiles : dev->num_sms;
     if (rope)
-        rc = bf16 ? launch_any<true, true>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
-                  : launch_any<false, true>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);
+        rc = bf16 ? launch_any<true, true, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
+                  : launch_any<false, true, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);
+    else if (pack_shift)
+        rc = bf16 ? launch_any<true, false, true>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
+                  : launch_any<false, false, true>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);
     else
-        rc = bf16 ? launch_any<true, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
-                  : launch_any<false, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);
+        rc = bf16 ? launch_any<true, false, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
+                  : launch_any<false, false, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);
     if (rc != ATTN_OK || splits == 1) return rc;
 
     // ---- merge the key ranges
@@ -446,19 +475,19 @@ int attn_fwd_f16(const void* q, const void* k, const void* v, void* o, float* ls
                          reinterpret_cast<cudaStream_t>(stream), false);
 }
 
-size_t attn_splitkv_workspace_bytes(int B, int Hq, int Sq, int Sk, int D, int num_splits) {
-    if (B < 0 || Hq < 0 || Sq < 0 || Sk < 0 || (D != 64 && D != 128) || num_splits < 0) return 0;
+size_t attn_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int D, int num_splits) {
+    if (B < 0 || Hq < 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || (D != 64 && D != 128) || num_splits < 0) return 0;
     int split_blocks = 1;
-    const int splits = resolve_splits(B, Hq, Sq, Sk, num_splits, &split_blocks);
+    const int splits = resolve_splits(B, Hq, Hkv, Sq, Sk, num_splits, false, &split_blocks);
     if (splits <= 1) return 0;
     size_t lse_off = 0;
     return workspace_layout(B, Hq, Sq, D, splits, &lse_off);
 }
 
-int attn_splitkv_num_splits(int B, int Hq, int Sq, int Sk, int num_splits) {
-    if (B < 0 || Hq < 0 || Sq < 0 || Sk < 0 || num_splits < 0) return 0;
+int attn_splitkv_num_splits(int B, int Hq, int Hkv, int Sq, int Sk, int num_splits) {
+    if (B < 0 || Hq < 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || num_splits < 0) return 0;
     int split_blocks = 1;
-    return resolve_splits(B, Hq, Sq, Sk, num_splits, &split_blocks);
+    return resolve_splits(B, Hq, Hkv, Sq, Sk, num_splits, false, &split_blocks);
 }
 
 int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
@@ -741,7 +770,7 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
                              int num_splits, attn_stream_t stream) {
     // Refuse, before anything else, a problem whose partial results would not
     // fit in the fixed scratch array.
-    if (attn_splitkv_workspace_bytes(B, Hq, Sq, Sk, D, num_splits) > kNoAllocScratchBytes)
+    if (attn_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, num_splits) > kNoAllocScratchBytes)
         return ATTN_ERR_UNSUPPORTED;
     DeviceInfo* dev = nullptr;
     int rc = device_info(&dev);

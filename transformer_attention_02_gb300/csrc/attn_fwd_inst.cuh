@@ -9,10 +9,10 @@
 
 namespace attn {
 
-template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE>
+template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE, bool PACK>
 int launch_fwd(bool& attr_set, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const FwdParams& p, int grid, cudaStream_t stream) {
-    auto kernel = attn_fwd_kernel<D, CAUSAL, ADDITIVE, BF16, ROPE>;
+    auto kernel = attn_fwd_kernel<D, CAUSAL, ADDITIVE, BF16, ROPE, PACK>;
     constexpr int smem = TileCfg<D>::kSmemBytes;
     if (!attr_set) {
         // The in-kernel register split assumes exactly kLaunchRegs per thread at launch.
@@ -29,17 +29,17 @@ int launch_fwd(bool& attr_set, const CUtensorMap& tq, const CUtensorMap& tk, con
 
 }  // namespace attn
 
-#define ATTN_INSTANTIATE_ONE(D, CAUSAL, ADDITIVE, BF16, ROPE)                                                  \
-    template int attn::launch_fwd<D, CAUSAL, ADDITIVE, BF16, ROPE>(bool&, const CUtensorMap&,                  \
-                                                                   const CUtensorMap&, const CUtensorMap&,     \
-                                                                   const attn::FwdParams&, int, cudaStream_t);
+#define ATTN_INSTANTIATE_ONE(D, CAUSAL, ADDITIVE, BF16, ROPE, PACK)                                              \
+    template int attn::launch_fwd<D, CAUSAL, ADDITIVE, BF16, ROPE, PACK>(bool&, const CUtensorMap&,              \
+                                                                         const CUtensorMap&, const CUtensorMap&, \
+                                                                         const attn::FwdParams&, int, cudaStream_t);
 
-#define ATTN_INSTANTIATE_FWD(BF16, ROPE)                  \
-    ATTN_INSTANTIATE_ONE(64, false, false, BF16, ROPE)    \
-    ATTN_INSTANTIATE_ONE(64, true, false, BF16, ROPE)     \
-    ATTN_INSTANTIATE_ONE(64, false, true, BF16, ROPE)     \
-    ATTN_INSTANTIATE_ONE(64, true, true, BF16, ROPE)      \
-    ATTN_INSTANTIATE_ONE(128, false, false, BF16, ROPE)   \
-    ATTN_INSTANTIATE_ONE(128, true, false, BF16, ROPE)    \
-    ATTN_INSTANTIATE_ONE(128, false, true, BF16, ROPE)    \
-    ATTN_INSTANTIATE_ONE(128, true, true, BF16, ROPE)
+#define ATTN_INSTANTIATE_FWD(BF16, ROPE, PACK)                  \
+    ATTN_INSTANTIATE_ONE(64, false, false, BF16, ROPE, PACK)    \
+    ATTN_INSTANTIATE_ONE(64, true, false, BF16, ROPE, PACK)     \
+    ATTN_INSTANTIATE_ONE(64, false, true, BF16, ROPE, PACK)     \
+    ATTN_INSTANTIATE_ONE(64, true, true, BF16, ROPE, PACK)      \
+    ATTN_INSTANTIATE_ONE(128, false, false, BF16, ROPE, PACK)   \
+    ATTN_INSTANTIATE_ONE(128, true, false, BF16, ROPE, PACK)    \
+    ATTN_INSTANTIATE_ONE(128, false, true, BF16, ROPE, PACK)    \
+    ATTN_INSTANTIATE_ONE(128, true, true, BF16, ROPE, PACK)

@@ -62,6 +62,9 @@ struct FwdParams {
     unsigned int* status;     // device status word, bit 0 = a wait timed out
     const float* rope;        // rotary table (max_pos, D/2, {cos, sin}) FP32 (rotating variant only)
     int q_pos0;               // position of query row 0 (rotating variant only)
+    // Kept last: inserting it earlier shifted the 64-bit fields after it and
+    // measurably changed the code generated for the unpacked kernels.
+    int pack_shift;           // > 0: the 2^pack_shift query heads of a K/V head share each tile's rows
 };
 
 constexpr int kThreads = 384;               // three warpgroups
@@ -123,7 +126,7 @@ struct TileCfg {
 };
 
 struct TileInfo {
-    int b, h, hk, m0;
+    int b, h, hk, m0;  // h: the (first) query head; m0: the first query row
     int split;      // key range index
     int kb0;        // first 128-key block of the key range
     int nb[2];      // KV blocks needed by query sub-tile t (rows m0+128t .. m0+128t+127)
@@ -133,9 +136,17 @@ struct TileInfo {
 // Work tiles in order: with a causal mask the longest first (query block
 // descending), and within one query block the (b, h) pairs in order, so the
 // query heads sharing a K/V head run side by side.
-template <bool CAUSAL>
+// With head packing (pack_shift > 0, decode and short prefills) a tile belongs
+// to one K/V head: each 128-row sub-tile holds 128 >> pack_shift query rows of
+// all 2^pack_shift query heads of the group (row r of the sub-tile is query
+// row r >> pack_shift of head h + (r & (group - 1))), so the group's heads
+// share every K/V block instead of streaming it once each.
+template <bool CAUSAL, bool PACK>
 __device__ __forceinline__ TileInfo tile_info(int tile, const FwdParams& p) {
-    const int bh_count = p.B * p.Hq;
+    const int ps = PACK ? p.pack_shift : 0;
+    const int heads = PACK ? p.Hkv : p.Hq;
+    const int sub_rows = kBlockM >> ps;
+    const int bh_count = p.B * heads;
     const int per_mb = bh_count * p.n_splits;
     const int mb_rank = tile / per_mb;
     const int rem = tile - mb_rank * per_mb;
@@ -143,18 +154,19 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const FwdParams& p) {
     const int bh = rem - split * bh_count;
     const int mb = CAUSAL ? (p.n_mblk - 1 - mb_rank) : mb_rank;
     TileInfo t;
-    t.b = bh / p.Hq;
-    t.h = bh - t.b * p.Hq;
-    t.hk = t.h / p.group;
-    t.m0 = mb * kRowsPerTile;
+    t.b = bh / heads;
+    const int hh = bh - t.b * heads;
+    t.h = PACK ? hh * p.group : hh;
+    t.hk = PACK ? hh : hh / p.group;
+    t.m0 = mb * 2 * sub_rows;
     t.split = split;
     t.kb0 = split * p.split_blocks;
     const int range_begin = t.kb0 * kBlockN;
     const int range_end = min(p.Sk, range_begin + p.split_blocks * kBlockN);
 #pragma unroll
     for (int s = 0; s < 2; ++s) {
-        const int first = t.m0 + s * kBlockM;
-        const int last = min(first + kBlockM - 1, p.Sq - 1);
+        const int first = t.m0 + s * sub_rows;
+        const int last = min(first + sub_rows - 1, p.Sq - 1);
         int kv_end = range_begin;
         if (first < p.Sq) kv_end = CAUSAL ? min(range_end, max(0, last + (p.Sk - p.Sq) + 1)) : range_end;
         t.nb[s] = kv_end > range_begin ? (kv_end - range_begin + kBlockN - 1) / kBlockN : 0;
@@ -215,7 +227,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const S
 // ------------------------------------------------------------ TMA producer
 // The whole warp runs this loop (so that addresses and coordinates stay
 // warp-uniform); lane 0 issues the copies.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool PACK>
 __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                          const FwdParams& p, uint32_t smem, const SyncCtx& sc) {
     using C = TileCfg<D>;
@@ -227,7 +239,7 @@ __device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const C
     for (int w = 0; w * (int)gridDim.x < p.n_tiles && alive; ++w) {
         const int tile = tile_of_wave(w);
         if (tile >= p.n_tiles) continue;
-        const TileInfo ti = tile_info<CAUSAL>(tile, p);
+        const TileInfo ti = tile_info<CAUSAL, PACK>(tile, p);
         if (ti.n == 0) continue;
         for (int j = 0; j < ti.n && alive; ++j) {
             for (int kv = 0; kv < 2; ++kv) {
@@ -332,12 +344,12 @@ __device__ __forceinline__ void rope_rotate_rows(uint8_t* tile, int r_begin, int
 }
 
 // Next work tile with at least one key block, from wave w0 on.
-template <bool CAUSAL>
+template <bool CAUSAL, bool PACK = false>
 __device__ bool next_work_tile(const FwdParams& p, int w0, int& w_out, TileInfo& t_out) {
     for (int w = w0; w * (int)gridDim.x < p.n_tiles; ++w) {
         const int tile = tile_of_wave(w);
         if (tile >= p.n_tiles) continue;
-        t_out = tile_info<CAUSAL>(tile, p);
+        t_out = tile_info<CAUSAL, PACK>(tile, p);
         if (t_out.n == 0) continue;
         w_out = w;
         return true;
@@ -376,7 +388,7 @@ __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr
 // one has finished with it; the upper sub-tile reuses one buffer and is fetched
 // while the previous tile's last products and epilogue run. In the rotary
 // variant this warp also rotates rows 0..63 of each sub-tile after it lands.
-template <int D, bool CAUSAL, bool BF16, bool ROPE>
+template <int D, bool CAUSAL, bool BF16, bool ROPE, bool PACK>
 __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t smem, uint8_t* smem_ptr,
                            const SyncCtx& sc) {
     using C = TileCfg<D>;
@@ -406,9 +418,10 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
         for (int w = 0; w * (int)gridDim.x < p.n_tiles; ++w) {
             const int tile = tile_of_wave(w);
             if (tile >= p.n_tiles) continue;
-            const TileInfo ti = tile_info<CAUSAL>(tile, p);
+            const TileInfo ti = tile_info<CAUSAL, PACK>(tile, p);
             if (ti.n == 0) continue;
-            if (!load(nq & 1, ti.m0, ti) || !load(2 + nq % C::kQ1Bufs, ti.m0 + kBlockM, ti)) break;
+            if (!load(nq & 1, ti.m0, ti) || !load(2 + nq % C::kQ1Bufs, ti.m0 + (kBlockM >> (PACK ? p.pack_shift : 0)), ti))
+                break;
             ++nq;
         }
     } else {
@@ -457,7 +470,7 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
 // O_t and overwrite P_t after it).
 // The whole warp runs the loop with warp-uniform descriptors; lane 0 issues
 // every MMA and every commit (a commit covers the MMAs of its own thread).
-template <int D, bool CAUSAL, bool BF16, bool ROPE>
+template <int D, bool CAUSAL, bool BF16, bool ROPE, bool PACK>
 __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const SyncCtx& sc) {
     using C = TileCfg<D>;
     const bool leader = (threadIdx.x & 31) == 0;
@@ -519,7 +532,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
     for (int w = 0; w * (int)gridDim.x < p.n_tiles && alive; ++w) {
         const int tile = tile_of_wave(w);
         if (tile >= p.n_tiles) continue;
-        const TileInfo ti = tile_info<CAUSAL>(tile, p);
+        const TileInfo ti = tile_info<CAUSAL, PACK>(tile, p);
         const int n = ti.n, n0 = ti.nb[0], n1 = ti.nb[1];     // n0, n1 are n or n - 1
         if (n == 0) continue;
         // Q buffers of this tile: lower sub-tile in buffer nq & 1 (its (nq >> 1)-th
@@ -574,7 +587,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
 }
 
 // ------------------------------------------------ softmax / epilogue warpgroup
-template <int D, bool CAUSAL, bool ADDITIVE, bool BF16>
+template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool PACK>
 __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, int wg, const SyncCtx& sc) {
     using C = TileCfg<D>;
     const uint32_t bars = smem + C::kBarOff;
@@ -591,15 +604,17 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
     for (int w = 0; w * (int)gridDim.x < p.n_tiles; ++w) {
         const int tile = tile_of_wave(w);
         if (tile >= p.n_tiles) continue;
-        const TileInfo ti = tile_info<CAUSAL>(tile, p);
+        const TileInfo ti = tile_info<CAUSAL, PACK>(tile, p);
         const int nb = ti.nb[wg];
-        const int row = ti.m0 + wg * kBlockM + r;
+        const int ps = PACK ? p.pack_shift : 0;
+        const int row = ti.m0 + ((wg * kBlockM + r) >> ps);                   // query row
+        const int hd = PACK ? ti.h + (r & ((1 << ps) - 1)) : ti.h;            // query head
         const bool row_ok = row < p.Sq;
-        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (((size_t)ti.b * p.Sq + row) * p.Hq + ti.h) * D;
-        float* lse_out = p.lse + ((size_t)ti.b * p.Hq + ti.h) * p.Sq + row;
+        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + (((size_t)ti.b * p.Sq + row) * p.Hq + hd) * D;
+        float* lse_out = p.lse + ((size_t)ti.b * p.Hq + hd) * p.Sq + row;
         // With split keys this tile's result goes to the FP32 partial buffers.
         const bool part = p.o_part != nullptr;
-        const size_t prow_index = (((size_t)ti.split * p.B + ti.b) * p.Hq + ti.h) * p.Sq + row;
+        const size_t prow_index = (((size_t)ti.split * p.B + ti.b) * p.Hq + hd) * p.Sq + row;
         float* prow = part ? p.o_part + prow_index * D : nullptr;
         if (part) lse_out = p.lse_part + prow_index;
         if (nb == 0) {                                        // no visible key for any row here
@@ -793,7 +808,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
 }
 
 // ------------------------------------------------------------------ kernel
-template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE>
+template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE, bool PACK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -833,15 +848,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 8) {
         ptx::setmaxnreg_inc<kSoftmaxRegs>();
-        role_softmax<D, CAUSAL, ADDITIVE, BF16>(p, smem, tmem, warp >> 2, sc);
+        role_softmax<D, CAUSAL, ADDITIVE, BF16, PACK>(p, smem, tmem, warp >> 2, sc);
     } else {
         ptx::setmaxnreg_dec<kControlRegs>();
         if (warp == kMmaWarp)
-            role_mma<D, CAUSAL, BF16, ROPE>(p, smem, tmem, sc);
+            role_mma<D, CAUSAL, BF16, ROPE, PACK>(p, smem, tmem, sc);
         else if (warp == kTmaWarp)
-            role_tma<D, CAUSAL>(&tmQ, &tmK, &tmV, p, smem, sc);
+            role_tma<D, CAUSAL, PACK>(&tmQ, &tmK, &tmV, p, smem, sc);
         else if (warp == kQWarp)
-            role_qload<D, CAUSAL, BF16, ROPE>(&tmQ, p, smem, smem_ptr, sc);
+            role_qload<D, CAUSAL, BF16, ROPE, PACK>(&tmQ, p, smem, smem_ptr, sc);
         else if (ROPE && warp == kRopeWarp)
             role_rope_q<D, CAUSAL, BF16>(p, smem, smem_ptr, sc);
         __syncwarp();

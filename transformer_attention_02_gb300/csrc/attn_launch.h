@@ -1,7 +1,7 @@
 // Host-side launchers of the compiled forward-kernel variants.
 //
 // Each variant (head dimension, causal mask, additive mask, 16-bit type,
-// rotary embedding of the queries) is compiled in one of the fwd_*.cu
+// rotary embedding of the queries, GQA head packing) is compiled in one of the fwd_*.cu
 // translation units, so that the variants build in parallel; the C ABI in
 // attn_api.cu reaches them only through launch_fwd.
 #pragma once
@@ -13,13 +13,13 @@ namespace attn {
 
 struct FwdParams;
 
-// Launches attn_fwd_kernel<D, CAUSAL, ADDITIVE, BF16, ROPE> with `grid`
+// Launches attn_fwd_kernel<D, CAUSAL, ADDITIVE, BF16, ROPE, PACK> with `grid`
 // persistent CTAs on `stream`. `attr_set` caches, per device, that the
 // variant's shared-memory attribute has been set and its register count
 // checked (the in-kernel register split needs exactly the launch count).
 // Returns ATTN_OK, ATTN_ERR_UNSUPPORTED (register count differs) or
 // ATTN_ERR_CUDA.
-template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE>
+template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE, bool PACK>
 int launch_fwd(bool& attr_set, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const FwdParams& p, int grid, cudaStream_t stream);
 

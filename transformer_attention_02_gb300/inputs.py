@@ -87,6 +87,14 @@ for _d in (64, 128):
 
 BENCH_CONFIG = "llama2_7b_prefill"
 
+# Decode over a KV cache (one new query row per sequence; split-key path):
+# Llama-3-8B-like GQA (32 query heads, 8 K/V heads of 128) and an MHA case.
+DECODE_CONFIGS = {
+    "gqa_decode": AttnConfig("gqa_decode", 16, 32, 8, 1, 8192, 128, causal=True),
+    "gqa_decode_long": AttnConfig("gqa_decode_long", 4, 32, 8, 1, 32768, 128, causal=True),
+    "mha_decode": AttnConfig("mha_decode", 16, 32, 32, 1, 4096, 128, causal=True),
+}
+
 
 def storage_dtype(name: str) -> torch.dtype:
     return {"bf16": torch.bfloat16, "f16": torch.float16}[name]
