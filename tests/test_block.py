@@ -64,7 +64,8 @@ def test_layernorm_matches_fp64(M, H):
     assert np.all(np.abs(got - exact) <= ulp), float(np.max(np.abs(got - exact) / ulp))
 
 
-@pytest.mark.parametrize("B,S,Hq,Hkv,D,causal", [(2, 300, 4, 2, 128, True), (1, 200, 8, 8, 64, False)])
+@pytest.mark.parametrize("B,S,Hq,Hkv,D,causal", [(2, 300, 4, 2, 128, True), (1, 200, 8, 8, 64, False),
+                                                 (2, 32, 8, 2, 128, True)])    # S * 4 <= 256: heads packed
 def test_packed_qkv_attention(B, S, Hq, Hkv, D, causal):
     qkv = _rand((B, S, (Hq + 2 * Hkv) * D), S + D)
     q = qkv[..., : Hq * D].reshape(B, S, Hq, D).contiguous()

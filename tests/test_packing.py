@@ -41,3 +41,26 @@ def test_packed_heads_match_oracle(case):
         o, lse = A.attention_splitkv(q.to(dev), k.to(dev), v.to(dev), causal=cfg.causal, mask=m, num_splits=ns)
     torch.cuda.synchronize()
     check(o, lse, q, k, v, mask, cfg.mask_kind, label=f"packed {case}")
+
+
+def test_long_kv_cache_decode():
+    """One query row against 262,144 cached keys (MQA, 8 query heads packed
+    into one tile per sequence, automatic key ranges)."""
+    cfg = I.AttnConfig("long_decode", 1, 8, 1, 1, 262144, 128, causal=True, seed=41)
+    q, k, v, _ = I.make_inputs(cfg)
+    dev = torch.device("cuda")
+    assert A.attn_splitkv_num_splits(1, 8, 1, 1, 262144, 0) > 1
+    o, lse = A.attention_splitkv(q.to(dev), k.to(dev), v.to(dev), causal=True, num_splits=0)
+    torch.cuda.synchronize()
+    check(o, lse, q, k, v, None, cfg.mask_kind, label="262k-key decode")
+
+
+def test_host_pipeline_on_packed_decode():
+    cfg = I.AttnConfig("host_decode", 4, 32, 8, 1, 2048, 128, causal=True, seed=43, dtype="f16")
+    q, k, v, _ = I.make_inputs(cfg)
+    dev = torch.device("cuda")
+    ref_o, ref_l = A.attention(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    o, lse = A.attention_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o.view(torch.int16), ref_o.cpu().view(torch.int16)) and torch.equal(lse, ref_l.cpu())
+    check(o, lse, q, k, v, None, cfg.mask_kind, label="host pipeline, packed decode")
