@@ -468,8 +468,12 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
 // first. Each commit covers every MMA issued before it, so "S_t ready" also
 // means that the previous O_t += P_t V has completed (the softmax may rescale
 // O_t and overwrite P_t after it).
-// The whole warp runs the loop with warp-uniform descriptors; lane 0 issues
-// every MMA and every commit (a commit covers the MMAs of its own thread).
+// Lane 0 alone runs the loop and issues every MMA and every commit (a commit
+// covers the MMAs of its own thread): a single thread needs no warp votes, and
+// the tensor core's queue is short, so every cycle the issuer spends between
+// two groups of MMAs can leave it idle. For the same reason the next K/V slot
+// is probed (without blocking) before a group is issued, and the wait after
+// the group is skipped when the probe already saw the slot full.
 template <int D, bool CAUSAL, bool BF16, bool ROPE, bool PACK>
 __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const SyncCtx& sc) {
     using C = TileCfg<D>;
@@ -489,12 +493,16 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
     bool alive = true;
     constexpr int kQReady = ROPE ? C::bQRdy : C::bQFull;   // Q usable once loaded (and rotated)
 
-    auto acquire = [&](uint32_t& slot) -> bool {      // next K or V tile of the ring
+    // Next K or V tile of the ring; `seen` = a probe already saw it full.
+    auto acquire = [&](uint32_t& slot, bool seen = false) -> bool {
         slot = kv_use % C::kSlots;
-        const bool ok = warp_wait(bar(C::bKVFull + slot), (kv_use / C::kSlots) & 1u, sc);
+        const bool ok = seen || wait_phase(bar(C::bKVFull + slot), (kv_use / C::kSlots) & 1u, sc);
         ++kv_use;
         if (ok) ptx::tc_fence_after_sync();
         return ok;
+    };
+    auto probe_next = [&]() -> bool {
+        return ptx::mbar_test_wait(bar(C::bKVFull + (int)(kv_use % C::kSlots)), (kv_use / C::kSlots) & 1u);
     };
     auto commit = [&](int b) {
         if (leader) ptx::tc_commit(bar(b));
@@ -522,13 +530,14 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         }
     };
     auto wait_p = [&](int t) -> bool {
-        const bool ok = warp_wait(bar(C::bPFull + t), p_cnt[t] & 1u, sc);
+        const bool ok = wait_phase(bar(C::bPFull + t), p_cnt[t] & 1u, sc);
         ++p_cnt[t];
         if (ok) ptx::tc_fence_after_sync();
         return ok;
     };
 
-    if (p.debug_stall) alive = warp_wait(bar(C::bStall), 0, sc);   // nothing ever arrives
+    if (!leader) return;
+    if (p.debug_stall) alive = wait_phase(bar(C::bStall), 0, sc);   // nothing ever arrives
     for (int w = 0; w * (int)gridDim.x < p.n_tiles && alive; ++w) {
         const int tile = tile_of_wave(w);
         if (tile >= p.n_tiles) continue;
@@ -545,25 +554,27 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
             commit(C::bQEmpty + q_buf[1]);
         };
         uint32_t ks, vs;
-        if (!warp_wait(bar(kQReady + q_buf[0]), (nq >> 1) & 1u, sc) || !acquire(ks)) { alive = false; break; }
+        if (!wait_phase(bar(kQReady + q_buf[0]), (nq >> 1) & 1u, sc) || !acquire(ks)) { alive = false; break; }
         if (n0 > 0) issue_qk(0, ks);
         issued = true;
-        if (!warp_wait(bar(kQReady + q_buf[1]), (nq / C::kQ1Bufs) & 1u, sc)) { alive = false; break; }
+        if (!wait_phase(bar(kQReady + q_buf[1]), (nq / C::kQ1Bufs) & 1u, sc)) { alive = false; break; }
         ptx::tc_fence_after_sync();
         ++nq;
         if (n1 > 0) issue_qk(1, ks);
         commit(C::bKVEmpty + ks);
         if (n == 1) release_q();
+        bool v_seen = false;
         for (int j = 0; j < n; ++j) {
             const bool more = j + 1 < n;
-            if (!acquire(vs)) { alive = false; break; }
+            if (!acquire(vs, v_seen)) { alive = false; break; }
+            const bool k_seen = more && probe_next();
             if (j < n0) {
                 if (!wait_p(0)) { alive = false; break; }
                 issue_pv(0, vs, j > 0);
                 if (j == n0 - 1) commit(C::bOFull + 0);
             }
             if (more) {
-                if (!acquire(ks)) { alive = false; break; }
+                if (!acquire(ks, k_seen)) { alive = false; break; }
                 if (j + 1 < n0) issue_qk(0, ks);
             }
             if (j < n1) {
@@ -573,6 +584,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
             }
             commit(C::bKVEmpty + vs);
             if (more) {
+                v_seen = probe_next();
                 if (j + 1 < n1) issue_qk(1, ks);
                 commit(C::bKVEmpty + ks);
                 if (j + 1 == n - 1) release_q();
