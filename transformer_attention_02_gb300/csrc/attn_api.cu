@@ -425,7 +425,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
         p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + lse_off);
     }
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.mask_vec4 = additive && aligned(mask, 16) && (Sk % 4 == 0);
+    p.mask_vec4 = !additive ? 0 : (aligned(mask, 32) && Sk % 8 == 0) ? 2 : (aligned(mask, 16) && Sk % 4 == 0) ? 1 : 0;
     p.o_vec8 = aligned(o, 32);
     p.debug_stall = g_debug_stall.load();
     p.timeout_ns = g_timeout_ns.load();

@@ -55,7 +55,7 @@ struct FwdParams {
     float* o_part;            // split keys: FP32 O of each key range (n_splits, B, Hq, Sq, D), else null
     float* lse_part;          // split keys: FP32 LSE of each key range (n_splits, B, Hq, Sq)
     float scale_log2;         // scale * log2(e)
-    int mask_vec4;            // mask rows may be read with 16-byte loads
+    int mask_vec4;            // mask rows may be read with 32-byte (2) or 16-byte (1) loads, else 0
     int o_vec8;               // O rows may be written with 32-byte stores
     int debug_stall;          // wait on a barrier nothing signals (timeout test)
     unsigned long long timeout_ns;
@@ -678,7 +678,17 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
 #pragma unroll
                     for (int c = 0; c < kBlockN; ++c) x[c] *= sl;
                     if (mrow != nullptr) {
-                        if (p.mask_vec4 && key0 + kBlockN <= p.Sk) {
+                        if (p.mask_vec4 == 2 && key0 + kBlockN <= p.Sk) {
+                            // Each lane reads its own row: 32-byte loads halve the cache lines
+                            // touched per load instruction compared with 16-byte ones.
+#pragma unroll
+                            for (int c = 0; c < kBlockN / 8; ++c) {
+                                float mv[8];
+                                ptx::ld_global_nc_v8(mrow + key0 + 8 * c, mv);
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) x[8 * c + i] = fmaf(mv[i], kLog2e, x[8 * c + i]);
+                            }
+                        } else if (p.mask_vec4 && key0 + kBlockN <= p.Sk) {
                             const float4* m4 = reinterpret_cast<const float4*>(mrow + key0);
 #pragma unroll
                             for (int c = 0; c < kBlockN / 4; ++c) {

@@ -252,6 +252,13 @@ __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r) {
                  : "memory");
 }
 
+// 32-byte read-only vector load from global memory (the address must be 32-byte aligned).
+__device__ __forceinline__ void ld_global_nc_v8(const float* ptr, float* r) {
+    asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7])
+                 : "l"(ptr));
+}
+
 // Per-warpgroup register budget (all four warps of a warpgroup execute it).
 template <uint32_t kRegs>
 __device__ __forceinline__ void setmaxnreg_inc() {
