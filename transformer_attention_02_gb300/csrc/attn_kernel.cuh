@@ -22,7 +22,8 @@
 //   warp  8    MMA issuer (one thread) + TMEM allocation
 //   warp  9    TMA producer of K/V (one thread) + barrier initialisation
 //   warp 10    TMA producer of Q (one thread), a tile ahead for the lower sub-tile
-//   warp 11    idle (it completes the third warpgroup for the register split)
+//   warp 11    idle (it completes the third warpgroup for the register split);
+//              in the rotary variant it rotates half of each Q sub-tile
 // Pipelining ("ops-transformer：…实战" §2.3): while one warpgroup exponentiates
 // its scores, the tensor cores work on the other warpgroup's tile, and the TMA
 // warp streams the next K/V tiles into a ring of shared-memory slots.
