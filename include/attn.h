@@ -86,7 +86,9 @@ typedef enum {
  *   mask_kind  one of attn_mask_kind; causal alignment is bottom-right
  *   mask  device, FP32, (B, Sq, Sk), broadcast over heads, 4-byte aligned;
  *         required for the additive kinds and ignored otherwise; -inf entries
- *         hide a key
+ *         hide a key. Rows are read with 32-byte loads when the mask is
+ *         32-byte aligned and Sk % 8 == 0 (16-byte loads when 16-byte aligned
+ *         and Sk % 4 == 0), which is faster; any 4-byte aligned mask works.
  *   stream     CUDA stream to enqueue on
  *   A pointer may be null only when its tensor has no elements (for example
  *   k and v when B or Sk is 0).
