@@ -33,9 +33,17 @@
  * Conventions shared by every entry point:
  *  - Pointers marked "device" are CUDA device addresses on the current device;
  *    "host" pointers are ordinary host memory. The caller owns every buffer.
- *  - The library allocates no device memory, keeps no per-call state and
- *    never synchronises implicitly: work is enqueued on `stream`
- *    (a cudaStream_t; NULL is the legacy default stream).
+ *  - No call allocates device memory (no cudaMalloc, no cudaFree), keeps
+ *    per-call state or synchronises implicitly: work is enqueued on `stream`
+ *    (a cudaStream_t; NULL is the legacy default stream). The library's
+ *    module does hold two fixed device arrays in every CUDA context that
+ *    loads it, for as long as the context lives: a 4-byte run-time status word
+ *    and the 32 MiB scratch array used only by attn_fwd_splitkv_noalloc.
+ *  - Per-context state (the status word's address, kernel attributes, the
+ *    host pipeline's streams) is cached per CUDA context, keyed by the
+ *    context's unique id, so the current context may be a device's primary
+ *    context or one the caller created; with no context current, the current
+ *    device's primary context is made current, as the CUDA runtime does.
  *  - Every argument is checked on the host before anything is launched; a
  *    rejected call launches nothing and writes nothing.
  *  - Return values are attn_status codes (0 = success), as in [GUIDE] §8.1's
@@ -180,10 +188,10 @@ size_t attn_splitkv_workspace_bytes(int B, int Hq, int Hkv, int Sq, int Sk, int 
  *   Limit: attn_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, num_splits) must not
  *   exceed 32 MiB (33554432 bytes); larger problems are refused with
  *   ATTN_ERR_UNSUPPORTED before anything is launched.
- *   The first call on each device looks up the array's device address on that
- *   device (cudaGetSymbolAddress, which may synchronise); make that first call
- *   before any stream capture.
- *   All calls on a device share the one array and it keeps the last call's
+ *   The first call in each CUDA context looks up the array's device address
+ *   in that context (cudaGetSymbolAddress, which may synchronise); make that
+ *   first call before any stream capture.
+ *   All calls in a context share the one array and it keeps the last call's
  *   contents. Nothing in it needs to start at zero (every partial result is
  *   written before it is read), but calls whose work overlaps on the GPU (for
  *   example on two streams at once) race on it: serialise them.

@@ -305,3 +305,25 @@ def test_block_arguments(lib, kw, code):
     a.update(kw)
     assert A.attn_block_fwd(a["x"], a["g"], a["b"], a["w_qkv"], a["b_qkv"], a["w_o"], a["b_o"], a["y"], a["B"], a["S"],
                             a["Hq"], a["Hkv"], a["D"], 1e-5, 1, a["ws"], a["ws_bytes"], None) == code
+
+
+def _noalloc(q=P, k=P, v=P, o=P, lse=P, B=4, Hq=32, Hkv=32, Sq=2048, Sk=2048, D=128, kind=1, mask=None,
+             splits=4):
+    return A.attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, 0.0, kind, mask, splits, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    # Invalid arguments on a problem too large for the scratch array are still
+    # reported as invalid (the same checks as attn_fwd_splitkv run first).
+    (dict(Hq=33, Hkv=2), A.ATTN_ERR_INVALID_ARG),
+    (dict(q=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(kind=5), A.ATTN_ERR_INVALID_ARG),
+    (dict(kind=2, mask=None), A.ATTN_ERR_INVALID_ARG),
+    (dict(o=P + 4), A.ATTN_ERR_INVALID_ARG),
+    (dict(splits=-1), A.ATTN_ERR_INVALID_ARG),
+    (dict(D=80), A.ATTN_ERR_UNSUPPORTED),
+    # Valid arguments whose partial results exceed the 32 MiB array.
+    (dict(), A.ATTN_ERR_UNSUPPORTED),
+])
+def test_noalloc_checks_arguments_before_the_scratch_limit(lib, kw, code):
+    assert _noalloc(**kw) == code

@@ -92,6 +92,8 @@ def test_long_context_config_sampled():
     check(o, lse, q, k, v, mask, cfg.mask_kind, slices=sl, rows=(0, 384), label="long head")
     check(o, lse, q, k, v, mask, cfg.mask_kind, slices=sl[:2], rows=(cfg.Sq - 256, cfg.Sq),
           label="long tail")
+    # the middle of the sequence: tiles that run mid-schedule
+    check(o, lse, q, k, v, mask, cfg.mask_kind, slices=sl, rows=(8064, 8448), label="long middle")
 
 
 @pytest.mark.parametrize("name", [n for n in I.CONFIGS if n.startswith("stress_")])

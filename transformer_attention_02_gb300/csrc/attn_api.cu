@@ -27,7 +27,7 @@ namespace {
 
 constexpr int kAbiVersion = 5;
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 
 std::atomic<unsigned long long> g_timeout_ns{kDefaultTimeoutNs};
 std::atomic<int> g_debug_stall{0};
@@ -35,57 +35,104 @@ std::atomic<int> g_debug_stall{0};
 // Run-time status word of each device: bit 0 = a bounded wait ran out.
 __device__ unsigned int g_device_status;
 
+// Cached state of one CUDA context (the primary context of a device, or a
+// context the caller created and made current). A __device__ symbol's address,
+// a function's attributes and the loaded module all belong to a context, so the
+// cache is keyed by the context's process-unique id, never reused.
 struct DeviceInfo {
+    unsigned long long ctx_id = 0;      // 0: free entry
     bool ready = false;
     bool supported = false;
     int num_sms = 0;
     unsigned int* status = nullptr;     // device address of g_device_status
+    void* noalloc_scratch = nullptr;    // device address of the allocation-free scratch array
     bool smem_attr_set[2][4][2][3] = {};   // [D is 128][mask kind][bf16][plain, rotary, packed]
     bool gemm_attr_set = false;
 };
 
 std::mutex g_mutex;
-DeviceInfo g_devices[kMaxDevices];
+DeviceInfo g_devices[kMaxContexts];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
 
-int fetch_encode_fn() {
-    if (g_encode) return ATTN_OK;
+template <typename Fn>
+bool fetch_driver_fn(const char* name, int version, Fn* out) {
+    if (*out) return true;
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
+    if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) != cudaSuccess ||
         q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return ATTN_ERR_CUDA;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    return ATTN_OK;
+        return false;
+    *out = reinterpret_cast<Fn>(fn);
+    return true;
 }
 
-// Current device's cached properties (sm_103 check, SM count, status word).
-int device_info(DeviceInfo** out) {
+// Process-unique id of the current context; makes the current device's
+// primary context current first when no context is (as the runtime would).
+int context_id_for(int dev, unsigned long long* id) {
+    if (!fetch_driver_fn("cuCtxGetCurrent", 4000, &g_ctx_current) || !fetch_driver_fn("cuCtxGetId", 12000, &g_ctx_id))
+        return ATTN_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS) return ATTN_ERR_CUDA;
+    if (ctx == nullptr) {
+        if (cudaSetDevice(dev) != cudaSuccess || g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+            return ATTN_ERR_CUDA;
+    }
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Cached properties of the current context (sm_103 check, SM count, status
+// word). The caller holds g_mutex.
+int device_info_locked(DeviceInfo** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    DeviceInfo& d = g_devices[dev];
-    if (!d.ready) {
+    unsigned long long id = 0;
+    int rc = context_id_for(dev, &id);
+    if (rc != ATTN_OK) return rc;
+    DeviceInfo* d = nullptr;
+    for (DeviceInfo& e : g_devices) {
+        if (e.ctx_id == id) { d = &e; break; }
+        if (!d && e.ctx_id == 0) d = &e;
+    }
+    if (d == nullptr) return ATTN_ERR_UNSUPPORTED;           // more live contexts than the cache holds
+    if (d->ctx_id != id) *d = DeviceInfo{};
+    d->ctx_id = id;
+    if (!d->ready) {
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return ATTN_ERR_CUDA;
-        d.supported = (major == 10 && minor == 3);
-        d.num_sms = sms;
-        if (d.supported) {
+        d->supported = (major == 10 && minor == 3);
+        d->num_sms = sms;
+        if (d->supported) {
             void* addr = nullptr;
             if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess) return ATTN_ERR_CUDA;
-            d.status = static_cast<unsigned int*>(addr);
-            if (fetch_encode_fn() != ATTN_OK) return ATTN_ERR_CUDA;
+            d->status = static_cast<unsigned int*>(addr);
+            if (!fetch_driver_fn("cuTensorMapEncodeTiled", 12000, &g_encode)) return ATTN_ERR_CUDA;
         }
-        d.ready = true;
+        d->ready = true;
     }
-    *out = &d;
-    return d.supported ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+    *out = d;
+    return d->supported ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
 }
+
+int device_info(DeviceInfo** out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    return device_info_locked(out);
+}
+
+}  // namespace
+
+int attn::current_context_id(unsigned long long* id) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    return context_id_for(dev, id);
+}
+
+namespace {
 
 // 4-D map over a (B, S, H, D) 16-bit tensor, innermost first: (D, H, S, B).
 // One box = 64 head-dim columns (128 bytes, the swizzle span) x 128 rows of S.
@@ -347,11 +394,11 @@ int launch_rope_apply(const void* x, void* y, int B, int S, int H, int D, const 
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                  int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, cudaStream_t stream,
-                  bool bf16, int num_splits = 1, void* workspace = nullptr, size_t workspace_bytes = 0,
-                  const RopeArgs* rope = nullptr, long long q_stride = 0, long long kv_stride = 0) {
-    // ---- arguments (host only, nothing enqueued yet)
+// Host-side checks of the arguments every forward entry point shares (all but
+// the workspace, which depends on the entry point). Nothing is enqueued.
+int check_fwd_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int Hq,
+                   int Hkv, int Sq, int Sk, int D, int mask_kind, const float* mask, int num_splits,
+                   const RopeArgs* rope) {
     if (B < 0 || Hq < 0 || Hkv <= 0 || Sq < 0 || Sk < 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
     if (mask_kind < ATTN_MASK_NONE || mask_kind > ATTN_MASK_CAUSAL_ADDITIVE) return ATTN_ERR_INVALID_ARG;
     const bool additive = mask_kind == ATTN_MASK_ADDITIVE || mask_kind == ATTN_MASK_CAUSAL_ADDITIVE;
@@ -367,14 +414,31 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     if (additive && !aligned(mask, 4)) return ATTN_ERR_INVALID_ARG;
     if (Sq > (1 << 30) || Sk > (1 << 30)) return ATTN_ERR_INVALID_ARG;
     if (rope && !rope_args_ok(*rope, Sq, Sk)) return ATTN_ERR_INVALID_ARG;
+    if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
     const int pack_shift = pack_shift_for(Hq, Hkv, Sq, rope != nullptr);
     const long long tile_heads = pack_shift ? Hkv : Hq;
     const long long rows_per_tile = attn::kRowsPerTile >> pack_shift;
     const long long n_mblk = ((long long)Sq + rows_per_tile - 1) / rows_per_tile;
-    if (num_splits < 0) return ATTN_ERR_INVALID_ARG;
     int split_blocks = 1;
     const int splits = resolve_splits(B, Hq, Hkv, Sq, Sk, num_splits, rope != nullptr, &split_blocks);
     if ((long long)B * tile_heads * n_mblk * splits > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                  int Sq, int Sk, int D, float scale, int mask_kind, const float* mask, cudaStream_t stream,
+                  bool bf16, int num_splits = 1, void* workspace = nullptr, size_t workspace_bytes = 0,
+                  const RopeArgs* rope = nullptr, long long q_stride = 0, long long kv_stride = 0) {
+    // ---- arguments (host only, nothing enqueued yet)
+    int rc = check_fwd_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mask_kind, mask, num_splits, rope);
+    if (rc != ATTN_OK) return rc;
+    const bool additive = mask_kind == ATTN_MASK_ADDITIVE || mask_kind == ATTN_MASK_CAUSAL_ADDITIVE;
+    const int pack_shift = pack_shift_for(Hq, Hkv, Sq, rope != nullptr);
+    const long long tile_heads = pack_shift ? Hkv : Hq;
+    const long long rows_per_tile = attn::kRowsPerTile >> pack_shift;
+    const long long n_mblk = ((long long)Sq + rows_per_tile - 1) / rows_per_tile;
+    int split_blocks = 1;
+    const int splits = resolve_splits(B, Hq, Hkv, Sq, Sk, num_splits, rope != nullptr, &split_blocks);
     if (B == 0 || Hq == 0 || Sq == 0) return ATTN_OK;        // nothing to compute
     size_t lse_off = 0;
     if (splits > 1) {
@@ -384,7 +448,7 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     if (!(scale > 0.f) || !std::isfinite(scale)) scale = 1.0f / std::sqrt((float)D);
 
     DeviceInfo* dev = nullptr;
-    int rc = device_info(&dev);
+    rc = device_info(&dev);
     if (rc != ATTN_OK) return rc;
 
     if (Sk == 0) {                                            // every row sees no key
@@ -742,22 +806,21 @@ namespace {
 // this library, held until the process exits, shared by every call.
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
-void* g_noalloc_scratch_ptr[kMaxDevices] = {};   // device address per device, guarded by g_mutex
 
-// Device address of the scratch array on the current device. In host code the
-// array's name is only a host-side stand-in, so its address must come from
-// cudaGetSymbolAddress, once per device, with that device current.
+// Device address of the scratch array in the current context. In host code
+// the array's name is only a host-side stand-in, so its address must come from
+// cudaGetSymbolAddress, once per context, with that context current.
 int noalloc_scratch(void** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_noalloc_scratch_ptr[dev]) {
+    DeviceInfo* d = nullptr;
+    int rc = device_info_locked(&d);
+    if (rc != ATTN_OK) return rc;
+    if (!d->noalloc_scratch) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return ATTN_ERR_CUDA;
-        g_noalloc_scratch_ptr[dev] = ptr;
+        d->noalloc_scratch = ptr;
     }
-    *out = g_noalloc_scratch_ptr[dev];
+    *out = d->noalloc_scratch;
     return ATTN_OK;
 }
 
@@ -768,13 +831,12 @@ extern "C" {
 int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                              int Hkv, int Sq, int Sk, int D, float scale, int mask_kind, const float* mask,
                              int num_splits, attn_stream_t stream) {
-    // Refuse, before anything else, a problem whose partial results would not
-    // fit in the fixed scratch array.
+    // The same argument checks as attn_fwd_splitkv first; then refuse a problem
+    // whose partial results would not fit in the fixed scratch array.
+    int rc = check_fwd_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, D, mask_kind, mask, num_splits, nullptr);
+    if (rc != ATTN_OK) return rc;
     if (attn_splitkv_workspace_bytes(B, Hq, Hkv, Sq, Sk, D, num_splits) > kNoAllocScratchBytes)
         return ATTN_ERR_UNSUPPORTED;
-    DeviceInfo* dev = nullptr;
-    int rc = device_info(&dev);
-    if (rc != ATTN_OK) return rc;
     void* scratch = nullptr;
     rc = noalloc_scratch(&scratch);
     if (rc != ATTN_OK) return rc;

@@ -21,15 +21,19 @@
 #include <mutex>
 
 #include "../../include/attn.h"
+#include "attn_launch.h"
 
 namespace {
 
 constexpr int kSlots = 3;
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 constexpr size_t kAlign = 256;
 constexpr int kTargetUnits = 8;       // enough units to overlap copies with compute
 
+// Streams and events of one CUDA context (they belong to the context that was
+// current when they were made), keyed by the context's process-unique id.
 struct Pipe {
+    unsigned long long ctx_id = 0;      // 0: free entry
     bool ready = false;
     cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
     cudaEvent_t start = nullptr;
@@ -37,13 +41,22 @@ struct Pipe {
 };
 
 std::mutex g_pipe_mutex;              // one enqueue at a time: the events are shared
-Pipe g_pipes[kMaxDevices];
+Pipe g_pipes[kMaxContexts];
 
 int pipe_for_current_device(Pipe** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
-    Pipe& p = g_pipes[dev];
+    unsigned long long id = 0;
+    if (attn::current_context_id(&id) != ATTN_OK) return ATTN_ERR_CUDA;
+    Pipe* slot = nullptr;
+    for (Pipe& e : g_pipes) {
+        if (e.ctx_id == id) { slot = &e; break; }
+        if (!slot && e.ctx_id == 0) slot = &e;
+    }
+    if (slot == nullptr) return ATTN_ERR_UNSUPPORTED;       // more live contexts than the cache holds
+    if (slot->ctx_id != id) *slot = Pipe{};
+    slot->ctx_id = id;
+    Pipe& p = *slot;
     if (!p.ready) {
         int major = 0, minor = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||

@@ -23,4 +23,9 @@ template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE, bool PACK>
 int launch_fwd(bool& attr_set, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                const FwdParams& p, int grid, cudaStream_t stream);
 
+// Process-unique id of the current CUDA context (the current device's primary
+// context is made current first when no context is). Per-context caches of the
+// library are keyed by it. Returns ATTN_OK or ATTN_ERR_CUDA.
+int current_context_id(unsigned long long* id);
+
 }  // namespace attn
