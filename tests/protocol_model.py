@@ -1,0 +1,671 @@
+"""Executable model of the attention kernel's synchronisation protocol.
+
+The fused kernel (transformer_attention_02_gb300/csrc/attn_kernel.cuh) runs
+five roles in one CTA that hand work to each other through shared-memory
+mbarriers: the K/V TMA producer, the Q TMA producer (and, in the rotary
+variant, a second rotating warp), the single-thread MMA issuer and two softmax
+warpgroups. This module re-states each role's control flow in Python, over the
+same tile schedule, and runs the roles under an adversarial scheduler together
+with the asynchronous agents they drive (TMA copies that land in any order,
+the tensor core's in-order queue of MMAs and commits).
+
+What it checks, on every interleaving it is given:
+  * no deadlock: some role or agent can always make progress until every role
+    has finished;
+  * every mbarrier wait is sound: a thread waiting for phase k of a barrier
+    (by its parity, as the hardware does) finds exactly k or k + 1 phases
+    completed; k - 1 would let the parity test pass before the phase it wants,
+    k + 2 would make it miss the phase (overrun);
+  * no data race on shared memory or tensor memory: a TMA copy never lands in
+    a ring slot or Q buffer that an unexecuted MMA still reads; every MMA reads
+    the K/V block, Q sub-tile (rotated, in the rotary variant) and P it
+    expects; S, P and O in tensor memory are written, read and rescaled in
+    the order the algorithm needs (the softmax reads S only after the Q K^T
+    that wrote it, rescales O only between two P V products, the epilogue
+    reads O after the tile's last P V and before the next tile's first one);
+  * the abort path terminates: when a bounded wait runs out (modelled by a
+    wait that nothing will ever satisfy, as the kernel's stall hook does),
+    every role leaves its loops and the shutdown waits (TMA copies landed,
+    MMAs retired) complete by themselves.
+
+The model is CPU-only test infrastructure; it shares no code with the kernel.
+"""
+from __future__ import annotations
+
+import random
+from collections import deque
+from dataclasses import dataclass, field
+
+
+class ProtocolError(AssertionError):
+    pass
+
+
+# ------------------------------------------------------------------ schedule
+
+BLOCK_M = 128
+BLOCK_N = 128
+ROWS_PER_TILE = 2 * BLOCK_M
+
+
+@dataclass
+class Params:
+    D: int = 128
+    causal: bool = True
+    B: int = 1
+    Hq: int = 2
+    Hkv: int = 2
+    Sq: int = 512
+    Sk: int = 512
+    num_splits: int = 1          # key ranges (split-key mode when > 1)
+    rope: bool = False           # rotary variant: Q rotated by two warps, "Q ready" has two arrivals
+    pack_shift: int = 0          # GQA head packing: 2^pack_shift query heads share a tile's rows
+    grid: int = 1                # persistent CTAs
+    cta: int = 0                 # which CTA of the grid is modelled
+    debug_stall: bool = False    # the MMA issuer first waits on a barrier nothing signals
+
+    @property
+    def slots(self) -> int:
+        return 4 if self.D == 128 else 8
+
+    @property
+    def q1_bufs(self) -> int:
+        return 1
+
+    @property
+    def q_bufs(self) -> int:
+        return 2 + self.q1_bufs
+
+
+@dataclass(frozen=True)
+class Tile:
+    b: int
+    h: int
+    hk: int
+    m0: int
+    split: int
+    kb0: int
+    nb: tuple
+    n: int
+
+
+def _ceil_div(a, b):
+    return (a + b - 1) // b
+
+
+def schedule(p: Params):
+    """The CTA's work tiles in order, as tile_info() and tile_of_wave() give them."""
+    ps = p.pack_shift
+    heads = p.Hkv if ps else p.Hq
+    group = p.Hq // p.Hkv
+    sub_rows = BLOCK_M >> ps
+    n_mblk = _ceil_div(p.Sq, ROWS_PER_TILE >> ps)
+    n_kb = _ceil_div(p.Sk, BLOCK_N)
+    split_blocks = _ceil_div(n_kb, p.num_splits) if p.num_splits > 1 else n_kb
+    n_splits = _ceil_div(n_kb, split_blocks) if p.num_splits > 1 else 1
+    n_tiles = p.B * heads * n_mblk * n_splits
+    out = []
+    w = 0
+    while w * p.grid < n_tiles:
+        tile = w * p.grid + ((p.grid - 1 - p.cta) if (w & 1) else p.cta)
+        w += 1
+        if tile >= n_tiles:
+            continue
+        bh_count = p.B * heads
+        per_mb = bh_count * n_splits
+        mb_rank, rem = divmod(tile, per_mb)
+        split, bh = divmod(rem, bh_count)
+        mb = (n_mblk - 1 - mb_rank) if p.causal else mb_rank
+        b, hh = divmod(bh, heads)
+        h = hh * group if ps else hh
+        hk = hh if ps else hh // group
+        m0 = mb * 2 * sub_rows
+        kb0 = split * split_blocks
+        begin = kb0 * BLOCK_N
+        end = min(p.Sk, begin + split_blocks * BLOCK_N)
+        nb = []
+        for s in range(2):
+            first = m0 + s * sub_rows
+            last = min(first + sub_rows - 1, p.Sq - 1)
+            kv_end = begin
+            if first < p.Sq:
+                kv_end = min(end, max(0, last + (p.Sk - p.Sq) + 1)) if p.causal else end
+            nb.append(_ceil_div(kv_end - begin, BLOCK_N) if kv_end > begin else 0)
+        out.append(Tile(b, h, hk, m0, split, kb0, tuple(nb), max(nb)))
+    return out
+
+
+# --------------------------------------------------------------- simulation
+
+class Barrier:
+    def __init__(self, name: str, count: int):
+        self.name = name
+        self.count = count
+        self.pending = count
+        self.tx = 0
+        self.completed = 0
+
+    def arrive(self):
+        self.pending -= 1
+        self._maybe_complete()
+
+    def expect_tx(self, n: int):
+        self.tx += n
+
+    def complete_tx(self, n: int):
+        self.tx -= n
+        self._maybe_complete()
+
+    def _maybe_complete(self):
+        if self.pending == 0 and self.tx == 0:
+            self.completed += 1
+            self.pending = self.count
+
+
+@dataclass
+class Proc:
+    name: str
+    gen: object
+    op: tuple = None
+    done: bool = False
+    blocked_since: int = 0
+
+
+@dataclass
+class Sim:
+    p: Params
+    rng: random.Random
+    timeouts: bool = False
+    bars: dict = field(default_factory=dict)
+    res: dict = field(default_factory=dict)
+    abort: bool = False
+    timed_out: bool = False
+    inflight: list = field(default_factory=list)
+    mma_queue: deque = field(default_factory=deque)
+    steps: int = 0
+
+    def bar(self, name: str) -> Barrier:
+        return self.bars[name]
+
+    # -- checks applied when a thread evaluates a wait
+    def poll(self, name: str, k: int) -> bool:
+        bar = self.bars[name]
+        c = bar.completed
+        if not self.abort and not (k <= c <= k + 1):
+            raise ProtocolError(f"{name}: waiting for phase {k} with {c} phases completed")
+        return (c & 1) != (k & 1)
+
+    def reads_pending(self, res_name: str) -> bool:
+        return any(res_name in item[1] for item in self.mma_queue if item[0] == "mma")
+
+    def tma_issue(self, bar: str, nbytes: int, res_name: str, tag):
+        if self.reads_pending(res_name):
+            raise ProtocolError(f"TMA into {res_name} while an unexecuted MMA still reads it")
+        st = self.res.get(res_name)
+        if isinstance(st, tuple) and st and st[0] == "loading":
+            raise ProtocolError(f"TMA into {res_name} while another copy into it is in flight")
+        self.res[res_name] = ("loading", tag)
+        self.inflight.append((bar, nbytes, res_name, tag))
+
+    def expect(self, res_name: str, want, what: str):
+        got = self.res.get(res_name)
+        if got != want:
+            raise ProtocolError(f"{what}: {res_name} holds {got}, expected {want}")
+
+
+def _tile_key(t: Tile):
+    return (t.b, t.h, t.m0, t.split)
+
+
+# ------------------------------------------------------------------ roles
+# Each role is a generator that yields the operations of the kernel role of
+# the same name, in the same order:
+#   ("wait", bar, phase)   bounded wait (returns False on abort or timeout)
+#   ("drain", bar, phase)  shutdown wait (ignores the abort flag)
+#   ("probe", bar, phase)  non-blocking test (returns the parity test)
+#   ("arrive", bar) / ("expect_tx", bar, bytes) / ("tma", bar, bytes, res, tag)
+#   ("mma", reads, fn) / ("commit", bar)   appended to the tensor core's queue
+#   ("act", fn)           a synchronous action of the thread (loads, stores)
+
+def role_tma(sim: Sim, tiles):
+    """K/V producer (warp 9): K_j then V_j of every block of every tile into the ring."""
+    p = sim.p
+    S = p.slots
+    kv_fill = 0
+    alive = True
+    for ti in tiles:
+        if not alive:
+            break
+        if ti.n == 0:
+            continue
+        for j in range(ti.n):
+            if not alive:
+                break
+            for kv in range(2):
+                slot = kv_fill % S
+                if kv_fill >= S:
+                    ok = yield ("wait", f"kv_empty{slot}", kv_fill // S - 1)
+                    if not ok:
+                        alive = False
+                        break
+                yield ("expect_tx", f"kv_full{slot}", 1)
+                yield ("tma", f"kv_full{slot}", 1, f"kv{slot}", ("KV", kv, ti.b, ti.hk, ti.kb0 + j))
+                kv_fill += 1
+    for s in range(S):
+        if kv_fill > s:
+            last = s + S * ((kv_fill - 1 - s) // S)
+            yield ("drain", f"kv_full{s}", last // S)
+
+
+def _q_tag(ti: Tile, t: int, p: Params):
+    return ("Q", ti.b, ti.h, ti.m0 + t * (BLOCK_M >> p.pack_shift))
+
+
+def _rotate(sim: Sim, buf: int, half: int):
+    def fn():
+        name = f"q{buf}"
+        st = sim.res.get(name)
+        if not (isinstance(st, tuple) and st and st[0] == "Q"):
+            raise ProtocolError(f"rotation of {name} before its copy landed ({st})")
+        if sim.reads_pending(name):
+            raise ProtocolError(f"rotation of {name} while an MMA reads it")
+        sim.res[name] = st + (("rot", half),)
+    return ("act", fn)
+
+
+def role_qload(sim: Sim, tiles):
+    """Q producer (warp 10); in the rotary variant it also rotates rows 0-63."""
+    p = sim.p
+    uses = [0] * p.q_bufs
+    nq = 0
+    work = [t for t in tiles if t.n > 0]
+
+    def load(buf, ti, t):
+        if uses[buf] > 0:
+            ok = yield ("wait", f"q_empty{buf}", uses[buf] - 1)
+            if not ok:
+                return False
+        yield ("expect_tx", f"q_full{buf}", 1)
+        yield ("tma", f"q_full{buf}", 1, f"q{buf}", _q_tag(ti, t, p))
+        uses[buf] += 1
+        return True
+
+    def rotate(buf, use):
+        ok = yield ("wait", f"q_full{buf}", use)
+        if not ok:
+            return False
+        yield _rotate(sim, buf, 0)
+        yield ("arrive", f"q_rdy{buf}")
+        return True
+
+    if not p.rope:
+        for ti in work:
+            if not (yield from load(nq & 1, ti, 0)):
+                break
+            if not (yield from load(2 + nq % p.q1_bufs, ti, 1)):
+                break
+            nq += 1
+    else:
+        idx = 0
+        have = bool(work) and (yield from load(0, work[0], 0))
+        lower_rotated = False
+        while have:
+            ti = work[idx]
+            b0, b1 = nq & 1, 2 + nq % p.q1_bufs
+            if not (yield from load(b1, ti, 1)):
+                break
+            more = idx + 1 < len(work)
+            if more and not (yield from load((nq + 1) & 1, work[idx + 1], 0)):
+                break
+            if not lower_rotated and not (yield from rotate(b0, nq >> 1)):
+                break
+            if not (yield from rotate(b1, nq // p.q1_bufs)):
+                break
+            if more and not (yield from rotate((nq + 1) & 1, (nq + 1) >> 1)):
+                break
+            lower_rotated = True
+            nq += 1
+            idx += 1
+            have = more
+    for b in range(p.q_bufs):
+        if uses[b] > 0:
+            yield ("drain", f"q_full{b}", uses[b] - 1)
+
+
+def role_rope_q(sim: Sim, tiles):
+    """Rotary variant, warp 11: rotates rows 64-127 of every Q sub-tile."""
+    p = sim.p
+    nq = 0
+    for ti in [t for t in tiles if t.n > 0]:
+        bufs = (nq & 1, 2 + nq % p.q1_bufs)
+        uses = (nq >> 1, nq // p.q1_bufs)
+        for t in range(2):
+            ok = yield ("wait", f"q_full{bufs[t]}", uses[t])
+            if not ok:
+                return
+            yield _rotate(sim, bufs[t], 1)
+            yield ("arrive", f"q_rdy{bufs[t]}")
+        nq += 1
+
+
+def _qk(sim: Sim, ti: Tile, t: int, q_buf: int, k_slot: int, blk: int):
+    """S_t = Q_t K_blk^T (an MMA group) as the tensor core executes it."""
+    p = sim.p
+    key = _tile_key(ti)
+    q_tag = _q_tag(ti, t, p)
+    if p.rope:
+        q_tag = q_tag + (("rot", 0), ("rot", 1))
+    k_tag = ("KV", 0, ti.b, ti.hk, ti.kb0 + blk)
+
+    def fn():
+        q_state = sim.res.get(f"q{q_buf}")
+        if not (isinstance(q_state, tuple) and q_state[:4] == q_tag[:4] and set(q_state[4:]) == set(q_tag[4:])):
+            raise ProtocolError(f"Q K^T of {key} sub-tile {t}: q{q_buf} holds {q_state}, expected {q_tag}")
+        sim.expect(f"kv{k_slot}", k_tag, f"Q K^T of {key} sub-tile {t} block {blk}")
+        s = sim.res.get(f"S{t}", "free")
+        if s != "free":
+            raise ProtocolError(f"Q K^T of {key} sub-tile {t} block {blk} overwrites S{t} holding {s}")
+        sim.res[f"S{t}"] = ("S", key, t, blk)
+    return ("mma", (f"q{q_buf}", f"kv{k_slot}"), fn)
+
+
+def _pv(sim: Sim, ti: Tile, t: int, v_slot: int, blk: int):
+    """O_t (+)= P_t V_blk as the tensor core executes it."""
+    key = _tile_key(ti)
+    v_tag = ("KV", 1, ti.b, ti.hk, ti.kb0 + blk)
+
+    def fn():
+        sim.expect(f"S{t}", ("P", key, t, blk), f"P V of {key} sub-tile {t} block {blk}")
+        sim.expect(f"kv{v_slot}", v_tag, f"P V of {key} sub-tile {t} block {blk}")
+        o = sim.res.get(f"O{t}", "free")
+        if blk == 0:
+            if not (o == "free" or (isinstance(o, tuple) and o[0] == "read")):
+                raise ProtocolError(f"first P V of {key} sub-tile {t} overwrites O{t} holding {o}")
+        elif o != ("O", key, t, blk - 1):
+            raise ProtocolError(f"P V of {key} sub-tile {t} block {blk}: O{t} holds {o}")
+        sim.res[f"S{t}"] = "free"
+        sim.res[f"O{t}"] = ("O", key, t, blk)
+    return ("mma", (f"S{t}", f"kv{v_slot}"), fn)
+
+
+def role_mma(sim: Sim, tiles):
+    """MMA issuer (warp 8, lane 0): the ping-pong issue order of role_mma."""
+    p = sim.p
+    S = p.slots
+    st = {"kv_use": 0}
+    p_cnt = [0, 0]
+    nq = 0
+    issued = False
+    alive = True
+    q_ready = "q_rdy" if p.rope else "q_full"
+
+    def acquire(seen=False):
+        slot = st["kv_use"] % S
+        ok = True
+        if not seen:
+            ok = yield ("wait", f"kv_full{slot}", st["kv_use"] // S)
+        st["kv_use"] += 1
+        return slot, ok
+
+    def probe_next():
+        u = st["kv_use"]
+        return (yield ("probe", f"kv_full{u % S}", u // S))
+
+    def wait_p(t):
+        ok = yield ("wait", f"p_full{t}", p_cnt[t])
+        p_cnt[t] += 1
+        return ok
+
+    if p.debug_stall:
+        alive = yield ("wait", "stall", 0)
+    for ti in tiles:
+        if not alive:
+            break
+        n, n0, n1 = ti.n, ti.nb[0], ti.nb[1]
+        if n == 0:
+            continue
+        q_buf = (nq & 1, 2 + nq % p.q1_bufs)
+        ok = yield ("wait", f"{q_ready}{q_buf[0]}", nq >> 1)
+        if ok:
+            ks, ok = yield from acquire()
+        if not ok:
+            alive = False
+            break
+        if n0 > 0:
+            yield _qk(sim, ti, 0, q_buf[0], ks, 0)
+            yield ("commit", "s_full0")
+        issued = True
+        ok = yield ("wait", f"{q_ready}{q_buf[1]}", nq // p.q1_bufs)
+        if not ok:
+            alive = False
+            break
+        nq += 1
+        if n1 > 0:
+            yield _qk(sim, ti, 1, q_buf[1], ks, 0)
+            yield ("commit", "s_full1")
+        yield ("commit", f"kv_empty{ks}")
+        if n == 1:
+            yield ("commit", f"q_empty{q_buf[0]}")
+            yield ("commit", f"q_empty{q_buf[1]}")
+        v_seen = False
+        for j in range(n):
+            more = j + 1 < n
+            vs, ok = yield from acquire(v_seen)
+            if not ok:
+                alive = False
+                break
+            k_seen = more and (yield from probe_next())
+            if j < n0:
+                if not (yield from wait_p(0)):
+                    alive = False
+                    break
+                yield _pv(sim, ti, 0, vs, j)
+                if j == n0 - 1:
+                    yield ("commit", "o_full0")
+            if more:
+                ks, ok = yield from acquire(k_seen)
+                if not ok:
+                    alive = False
+                    break
+                if j + 1 < n0:
+                    yield _qk(sim, ti, 0, q_buf[0], ks, j + 1)
+                    yield ("commit", "s_full0")
+            if j < n1:
+                if not (yield from wait_p(1)):
+                    alive = False
+                    break
+                yield _pv(sim, ti, 1, vs, j)
+                if j == n1 - 1:
+                    yield ("commit", "o_full1")
+            yield ("commit", f"kv_empty{vs}")
+            if more:
+                v_seen = yield from probe_next()
+                if j + 1 < n1:
+                    yield _qk(sim, ti, 1, q_buf[1], ks, j + 1)
+                    yield ("commit", "s_full1")
+                yield ("commit", f"kv_empty{ks}")
+                if j + 1 == n - 1:
+                    yield ("commit", f"q_empty{q_buf[0]}")
+                    yield ("commit", f"q_empty{q_buf[1]}")
+    if issued:
+        yield ("commit", "drain")
+        yield ("drain", "drain", 0)
+
+
+def role_softmax(sim: Sim, tiles, t: int):
+    """Softmax warpgroup t: per block, S_t -> P_t (rescaling O_t), then the epilogue."""
+    s_cnt = 0
+    o_cnt = 0
+    for ti in tiles:
+        nb = ti.nb[t]
+        key = _tile_key(ti)
+        if nb == 0:
+            continue
+        ok = True
+        for j in range(nb):
+            landed = yield ("wait", f"s_full{t}", s_cnt)
+            s_cnt += 1
+            if landed:
+                def fn(j=j):
+                    sim.expect(f"S{t}", ("S", key, t, j), f"softmax {t} block {j}")
+                    if j > 0:      # the lazy rescale of O_t may run here
+                        sim.expect(f"O{t}", ("O", key, t, j - 1), f"rescale of O{t} at block {j}")
+                    sim.res[f"S{t}"] = ("P", key, t, j)
+                yield ("act", fn)
+            ok = landed
+            if not ok:
+                break
+            yield ("arrive", f"p_full{t}")
+        if not ok:
+            return
+        ok = yield ("wait", f"o_full{t}", o_cnt)
+        if not ok:
+            return
+        o_cnt += 1
+
+        def epi(nb=nb):
+            sim.expect(f"O{t}", ("O", key, t, nb - 1), f"epilogue {t}")
+            sim.res[f"O{t}"] = ("read", key, t)
+        yield ("act", epi)
+
+
+# ---------------------------------------------------------------- scheduler
+
+def make_sim(p: Params, seed: int, timeouts: bool = False):
+    sim = Sim(p, random.Random(seed), timeouts=timeouts)
+    names = [("q_full", p.q_bufs, 1), ("q_empty", p.q_bufs, 1), ("s_full", 2, 1), ("p_full", 2, 1),
+             ("o_full", 2, 1), ("kv_full", p.slots, 1), ("kv_empty", p.slots, 1), ("q_rdy", p.q_bufs, 2)]
+    for base, n, count in names:
+        for i in range(n):
+            sim.bars[f"{base}{i}"] = Barrier(f"{base}{i}", count)
+    sim.bars["drain"] = Barrier("drain", 1)
+    sim.bars["stall"] = Barrier("stall", 1)
+    tiles = schedule(p)
+    procs = [Proc("tma", role_tma(sim, tiles)), Proc("qload", role_qload(sim, tiles)),
+             Proc("mma", role_mma(sim, tiles)), Proc("softmax0", role_softmax(sim, tiles, 0)),
+             Proc("softmax1", role_softmax(sim, tiles, 1))]
+    if p.rope:
+        procs.append(Proc("rope_q", role_rope_q(sim, tiles)))
+    return sim, procs, tiles
+
+
+def _advance(proc: Proc, value=None):
+    try:
+        proc.op = proc.gen.send(value) if proc.op is not None else next(proc.gen)
+    except StopIteration:
+        proc.done = True
+        proc.op = None
+
+
+def run(p: Params, seed: int = 0, timeouts: bool = False, bias: float = 0.5, max_steps: int = 2_000_000,
+        abort_at: int = None):
+    """One adversarially scheduled execution. Raises ProtocolError on a
+    violation or a deadlock; returns the simulation state at the end.
+
+    timeouts: a bounded wait that nothing can satisfy runs out (sets the
+    abort flag) instead of being reported as a deadlock.
+    abort_at: at that step some wait of the CTA is taken to have run out (the
+    abort flag is raised wherever the roles are)."""
+    sim, procs, tiles = make_sim(p, seed, timeouts)
+    rng = sim.rng
+    for pr in procs:
+        _advance(pr)
+    # per-run priorities: some agents run eagerly, others lag behind
+    prio = {pr.name: rng.random() for pr in procs}
+    prio["tma_agent"] = rng.random()
+    prio["mma_agent"] = rng.random()
+
+    def runnable(pr: Proc):
+        op = pr.op
+        kind = op[0]
+        if kind == "wait":
+            if sim.abort:
+                return True
+            return sim.poll(op[1], op[2])
+        if kind == "drain":
+            return sim.poll(op[1], op[2])
+        return True
+
+    while True:
+        if all(pr.done for pr in procs):
+            break                               # every thread has left: the kernel ends here
+        sim.steps += 1
+        if abort_at is not None and sim.steps == abort_at:
+            sim.abort = True
+            sim.timed_out = True
+        if sim.steps > max_steps:
+            raise ProtocolError("step limit reached (livelock?)")
+        cands = [("proc", pr) for pr in procs if not pr.done and runnable(pr)]
+        cands += [("tma", i) for i in range(len(sim.inflight))]
+        if sim.mma_queue:
+            cands.append(("mma", None))
+        if not cands:
+            blocked = [pr for pr in procs if not pr.done]
+            waiting = [pr for pr in blocked if pr.op[0] == "wait"]
+            if sim.timeouts and waiting:
+                pr = rng.choice(waiting)          # the bounded wait runs out
+                sim.abort = True
+                sim.timed_out = True
+                _advance(pr, False)
+                continue
+            raise ProtocolError("deadlock: " + ", ".join(f"{pr.name} at {pr.op}" for pr in blocked))
+        # biased choice: prefer high-priority candidates, sometimes pick uniformly
+        if rng.random() < bias:
+            def weight(c):
+                if c[0] == "proc":
+                    return prio[c[1].name]
+                return prio["tma_agent"] if c[0] == "tma" else prio["mma_agent"]
+            kind, obj = max(cands, key=lambda c: weight(c) + 0.3 * rng.random())
+        else:
+            kind, obj = rng.choice(cands)
+        if kind == "tma":
+            bar, nbytes, res_name, tag = sim.inflight.pop(obj)
+            sim.res[res_name] = tag
+            sim.bars[bar].complete_tx(nbytes)
+            continue
+        if kind == "mma":
+            item = sim.mma_queue.popleft()
+            if item[0] == "mma":
+                item[2]()
+            else:
+                sim.bars[item[1]].arrive()
+            continue
+        pr = obj
+        op = pr.op
+        k = op[0]
+        val = None
+        if k == "wait":
+            # satisfied, or (after an abort) whatever the last poll of wait_phase saw
+            val = sim.poll(op[1], op[2])
+        elif k == "drain":
+            val = True
+        elif k == "probe":
+            val = sim.poll(op[1], op[2])
+        elif k == "arrive":
+            sim.bars[op[1]].arrive()
+        elif k == "expect_tx":
+            sim.bars[op[1]].expect_tx(op[2])
+            sim.bars[op[1]].arrive()
+        elif k == "tma":
+            sim.tma_issue(op[1], op[2], op[3], op[4])
+        elif k == "mma":
+            sim.mma_queue.append(op)
+        elif k == "commit":
+            sim.mma_queue.append(("commit", op[1]))
+        elif k == "act":
+            op[1]()
+        else:
+            raise ProtocolError(f"unknown op {op}")
+        _advance(pr, val)
+
+    if not sim.abort:
+        if sim.inflight or sim.mma_queue:
+            raise ProtocolError("kernel ended with copies or MMAs in flight")
+        for t in range(2):
+            o = sim.res.get(f"O{t}", "free")
+            if not (o == "free" or o[0] == "read"):
+                raise ProtocolError(f"O{t} not read out at the end: {o}")
+    else:
+        if sim.inflight or sim.mma_queue:
+            raise ProtocolError("abort path ended with copies or MMAs in flight")
+    return sim

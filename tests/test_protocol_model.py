@@ -1,0 +1,175 @@
+"""The attention kernel's barrier protocol, checked on the CPU.
+
+tests/protocol_model.py re-states every role of the kernel (K/V and Q
+producers, the rotating warp of the rotary variant, the MMA issuer, the two
+softmax warpgroups) and runs them under many adversarial schedules together
+with the asynchronous TMA copies and the tensor core's in-order MMA queue. The
+cases cover both head dimensions (ring of 4 and 8 slots), causal and
+non-causal tiles with ragged tails and Sq != Sk, sub-tiles with no key block,
+GQA head packing, split-key mode, the rotary variant's two-arrival "Q ready"
+barriers, and the abort path (a stalled wait that runs out; an abort raised at
+an arbitrary moment). Planted protocol mistakes must each be caught.
+"""
+import os
+import sys
+import types
+
+import pytest
+
+import protocol_model as M
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+CASES = [
+    M.Params(),                                                        # causal, ring of 4
+    M.Params(D=64),                                                    # ring of 8
+    M.Params(causal=False, Sq=300, Sk=700),                            # ragged, upper sub-tile empty
+    M.Params(Sq=1000, Sk=300),                                         # Sq > Sk: lower sub-tiles with no block
+    M.Params(Sq=100, Sk=1000),
+    M.Params(B=2, Hq=4, Hkv=2, Sq=1200, Sk=1200, grid=3, cta=2),        # snake waves, mixed lengths
+    M.Params(B=2, Hq=4, Hkv=2, Sq=1200, Sk=1200, grid=3, cta=0, D=64),
+    M.Params(num_splits=3, Sq=100, Sk=1500, grid=2, cta=1),            # split keys
+    M.Params(num_splits=4, Sq=1, Sk=2000, Hq=8, Hkv=2, pack_shift=2, grid=2, cta=0),   # packed decode
+    M.Params(Hq=8, Hkv=2, pack_shift=2, Sq=40, Sk=900),
+    M.Params(rope=True),                                               # two-arrival "Q ready"
+    M.Params(rope=True, D=64, causal=False, Sq=600, Sk=500),
+    M.Params(rope=True, B=2, Hq=2, Hkv=1, Sq=700, Sk=700, grid=2, cta=1),
+    M.Params(Sq=128, Sk=128, Hq=1, Hkv=1),                             # one block per tile
+    M.Params(Sq=256, Sk=256, Hq=3, Hkv=3, causal=False),
+]
+
+SEEDS = range(12)
+
+
+def _id(p):
+    return f"D{p.D}_c{int(p.causal)}_B{p.B}H{p.Hq}-{p.Hkv}_S{p.Sq}-{p.Sk}_sp{p.num_splits}_r{int(p.rope)}" \
+           f"_pk{p.pack_shift}_g{p.grid}.{p.cta}"
+
+
+@pytest.mark.parametrize("p", CASES, ids=_id)
+def test_protocol_has_no_deadlock_or_race(p):
+    assert M.schedule(p), "the case must give the CTA some work"
+    for seed in SEEDS:
+        M.run(p, seed=seed, bias=(seed % 4) / 4)
+
+
+@pytest.mark.parametrize("p", [CASES[0], CASES[1], CASES[7], CASES[10]], ids=_id)
+def test_stalled_wait_aborts_every_role(p):
+    """The stall hook: the MMA issuer waits on a barrier nothing signals; its
+    wait runs out, and every role must then finish, shutdown waits included."""
+    stalled = M.Params(**{**p.__dict__, "debug_stall": True})
+    for seed in SEEDS:
+        sim = M.run(stalled, seed=seed, timeouts=True)
+        assert sim.timed_out
+
+
+@pytest.mark.parametrize("p", [CASES[0], CASES[2], CASES[5], CASES[11]], ids=_id)
+def test_abort_at_any_moment_terminates(p):
+    """Some wait runs out at an arbitrary step: no role may hang afterwards."""
+    total = M.run(p, seed=0).steps
+    for seed in SEEDS:
+        for frac in (0.05, 0.3, 0.6, 0.9):
+            M.run(p, seed=seed, abort_at=max(2, int(total * frac)), timeouts=True)
+
+
+# ------------------------------------------------------------ planted bugs
+
+MUTATIONS = {
+    # the MMA issuer never releases a ring slot after the V products
+    "kv_empty_commit_dropped": ('            yield ("commit", f"kv_empty{vs}")\n', ""),
+    # the producer waits for the slot's current phase instead of the previous one
+    "ring_wait_wrong_phase": ('ok = yield ("wait", f"kv_empty{slot}", kv_fill // S - 1)',
+                              'ok = yield ("wait", f"kv_empty{slot}", kv_fill // S)'),
+    # the producer reuses a slot without waiting for its release
+    "ring_wait_skipped": ("                if kv_fill >= S:\n", "                if False:\n"),
+    # V before K in the ring: the issuer takes the wrong tiles
+    "ring_order_swapped": ('("KV", kv, ti.b, ti.hk, ti.kb0 + j)', '("KV", 1 - kv, ti.b, ti.hk, ti.kb0 + j)'),
+    # Q buffers released one block early
+    "q_release_early": ("                if j + 1 == n - 1:\n", "                if j + 2 == n - 1 or (n == 2 and j == 0):\n"),
+    # the next S_t written before P_t has been consumed
+    "qk_before_pv": (
+        "            if j < n0:\n"
+        "                if not (yield from wait_p(0)):\n"
+        "                    alive = False\n"
+        "                    break\n"
+        "                yield _pv(sim, ti, 0, vs, j)\n"
+        "                if j == n0 - 1:\n"
+        "                    yield (\"commit\", \"o_full0\")\n"
+        "            if more:\n"
+        "                ks, ok = yield from acquire(k_seen)\n"
+        "                if not ok:\n"
+        "                    alive = False\n"
+        "                    break\n"
+        "                if j + 1 < n0:\n"
+        "                    yield _qk(sim, ti, 0, q_buf[0], ks, j + 1)\n"
+        "                    yield (\"commit\", \"s_full0\")\n",
+        "            if more:\n"
+        "                ks, ok = yield from acquire(k_seen)\n"
+        "                if not ok:\n"
+        "                    alive = False\n"
+        "                    break\n"
+        "                if j + 1 < n0:\n"
+        "                    yield _qk(sim, ti, 0, q_buf[0], ks, j + 1)\n"
+        "                    yield (\"commit\", \"s_full0\")\n"
+        "            if j < n0:\n"
+        "                if not (yield from wait_p(0)):\n"
+        "                    alive = False\n"
+        "                    break\n"
+        "                yield _pv(sim, ti, 0, vs, j)\n"
+        "                if j == n0 - 1:\n"
+        "                    yield (\"commit\", \"o_full0\")\n"),
+    # "O ready" committed before the last P V product
+    "o_full_early": ("                yield _pv(sim, ti, 0, vs, j)\n                if j == n0 - 1:\n"
+                     "                    yield (\"commit\", \"o_full0\")",
+                     "                if j == n0 - 1:\n                    yield (\"commit\", \"o_full0\")\n"
+                     "                yield _pv(sim, ti, 0, vs, j)"),
+    # the softmax does not wait for S
+    "softmax_skips_s_wait": ('            landed = yield ("wait", f"s_full{t}", s_cnt)',
+                             '            landed = True'),
+    # "Q ready" of the rotary variant with one arrival instead of two
+    "rope_ready_one_arrival": ('("q_rdy", p.q_bufs, 2)', '("q_rdy", p.q_bufs, 1)'),
+    # the softmax counts its S phases per tile instead of continuously
+    "softmax_phase_reset": ("        ok = True\n        for j in range(nb):", "        ok = True\n        s_cnt = 0\n        for j in range(nb):"),
+    # the issuer waits for Q of the upper sub-tile on the lower sub-tile's buffer
+    "q_buffer_mixup": ('ok = yield ("wait", f"{q_ready}{q_buf[1]}", nq // p.q1_bufs)',
+                       'ok = yield ("wait", f"{q_ready}{q_buf[0]}", nq >> 1)'),
+    # the K/V producer stops draining its copies on shutdown
+    "drain_skipped": ('            yield ("drain", f"kv_full{s}", last // S)', "            pass"),
+}
+
+MUTATION_CASES = [CASES[0], CASES[1], CASES[2], CASES[5], CASES[7], CASES[10], CASES[12]]
+
+
+def _mutant(name):
+    src = open(os.path.join(HERE, "protocol_model.py")).read()
+    old, new = MUTATIONS[name]
+    assert src.count(old) >= 1, f"mutation {name} no longer applies"
+    mod = types.ModuleType(f"protocol_model_{name}")
+    sys.modules[mod.__name__] = mod            # dataclasses look their module up
+    exec(compile(src.replace(old, new), f"<mutant {name}>", "exec"), mod.__dict__)
+    return mod
+
+
+def _caught(mod, **kw):
+    try:
+        mod.run(**kw)
+    except mod.ProtocolError:
+        return True
+    return False
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_protocol_bug_is_caught(name):
+    mod = _mutant(name)
+    for p in MUTATION_CASES:
+        q = mod.Params(**p.__dict__)
+        for seed in SEEDS:
+            if _caught(mod, p=q, seed=seed, bias=(seed % 4) / 4):
+                return
+    for p in MUTATION_CASES[:3]:                       # shutdown mistakes show on the abort path
+        q = mod.Params(**p.__dict__)
+        total = M.run(p, seed=0).steps
+        for seed in SEEDS:
+            if _caught(mod, p=q, seed=seed, timeouts=True, abort_at=max(2, int(total * (seed + 1) / 14))):
+                return
+    pytest.fail(f"planted protocol bug {name!r} was not detected")
