@@ -63,6 +63,15 @@ class Params:
     grid: int = 1                # persistent CTAs
     cta: int = 0                 # which CTA of the grid is modelled
     debug_stall: bool = False    # the MMA issuer first waits on a barrier nothing signals
+    tile_slots: int = 8          # entries of the shared-memory tile ring
+    steal_seed: int = -1         # >= 0: the CTA's tiles are its own and a random set taken over from CTAs
+                                 # that had not started (cluster launch control), in launch order
+
+    @property
+    def tile_consumers(self) -> int:
+        """Arrivals that free a tile-ring entry: the K/V producer, the MMA
+        issuer, the eight softmax warps and, in the rotary variant, warp 11."""
+        return 1 + 1 + 8 + (1 if self.rope else 0)
 
     @property
     def slots(self) -> int:
@@ -94,7 +103,11 @@ def _ceil_div(a, b):
 
 
 def schedule(p: Params):
-    """The CTA's work tiles in order, as tile_info() and tile_of_wave() give them."""
+    """The CTA's work tiles in order. One CTA per tile is launched and each CTA
+    starts with its own tile (blockIdx.x = cta) and then takes over tiles of
+    CTAs that had not started, always in launch order: the model uses either
+    the back-and-forth wave order of a persistent grid (steal_seed < 0) or a
+    random increasing subset of the later tiles."""
     ps = p.pack_shift
     heads = p.Hkv if ps else p.Hq
     group = p.Hq // p.Hkv
@@ -105,10 +118,16 @@ def schedule(p: Params):
     n_splits = _ceil_div(n_kb, split_blocks) if p.num_splits > 1 else 1
     n_tiles = p.B * heads * n_mblk * n_splits
     out = []
-    w = 0
-    while w * p.grid < n_tiles:
-        tile = w * p.grid + ((p.grid - 1 - p.cta) if (w & 1) else p.cta)
-        w += 1
+    if p.steal_seed >= 0:
+        rng = random.Random(p.steal_seed)
+        order = [p.cta] + sorted(t for t in range(p.cta + 1, n_tiles) if rng.random() < 0.4)
+    else:
+        order = []
+        w = 0
+        while w * p.grid < n_tiles:
+            order.append(w * p.grid + ((p.grid - 1 - p.cta) if (w & 1) else p.cta))
+            w += 1
+    for tile in order:
         if tile >= n_tiles:
             continue
         bh_count = p.B * heads
@@ -217,6 +236,53 @@ def _tile_key(t: Tile):
     return (t.b, t.h, t.m0, t.split)
 
 
+# ---------------------------------------------------------------- tile ring
+# The Q warp computes each work tile once and publishes it in a ring of
+# shared-memory entries (tile_full[slot], one arrival); every other role reads
+# the entries in order and frees each one as soon as it holds a copy
+# (tile_empty[slot], one arrival per consumer). After the last tile the
+# producer publishes an end marker (None).
+
+def ring_entries(tiles):
+    return list(tiles) + [None]
+
+
+def ring_fetch(sim: Sim, k: int, arrivals: int = 1):
+    """Consumer side: wait for entry k, copy it, free it."""
+    p = sim.p
+    slot = k % p.tile_slots
+    ok = yield ("wait", f"tile_full{slot}", k // p.tile_slots)
+    if not ok:
+        return False, None
+    box = {}
+
+    def read():
+        got = sim.res.get(f"tile{slot}")
+        if got is None or got[0] != k:
+            raise ProtocolError(f"tile ring slot {slot}: entry {got and got[0]} read as entry {k}")
+        box["t"] = got[1]
+    yield ("act", read)
+    for _ in range(arrivals):
+        yield ("arrive", f"tile_empty{slot}")
+    return True, box["t"]
+
+
+def ring_produce(sim: Sim, k: int, entry, waited: bool = False):
+    """Producer side: wait until entry k - slots has been freed, write entry k."""
+    p = sim.p
+    slot = k % p.tile_slots
+    if k >= p.tile_slots and not waited:
+        ok = yield ("wait", f"tile_empty{slot}", k // p.tile_slots - 1)
+        if not ok:
+            return False
+
+    def write():
+        sim.res[f"tile{slot}"] = (k, entry)
+    yield ("act", write)
+    yield ("arrive", f"tile_full{slot}")
+    return True
+
+
 # ------------------------------------------------------------------ roles
 # Each role is a generator that yields the operations of the kernel role of
 # the same name, in the same order:
@@ -228,29 +294,38 @@ def _tile_key(t: Tile):
 #   ("act", fn)           a synchronous action of the thread (loads, stores)
 
 def role_tma(sim: Sim, tiles):
-    """K/V producer (warp 9): K_j then V_j of every block of every tile into the ring."""
+    """K/V producer (warp 9): the blocks in the order the MMA issuer takes
+    them, K_0, then per block V_j and K_{j+1}; work tiles from the tile ring."""
     p = sim.p
     S = p.slots
-    kv_fill = 0
-    alive = True
-    for ti in tiles:
-        if not alive:
+    st = {"fill": 0, "alive": True}
+
+    def load(kv, ti, blk):
+        slot = st["fill"] % S
+        if st["fill"] >= S:
+            ok = yield ("wait", f"kv_empty{slot}", st["fill"] // S - 1)
+            if not ok:
+                st["alive"] = False
+                return
+        yield ("expect_tx", f"kv_full{slot}", 1)
+        yield ("tma", f"kv_full{slot}", 1, f"kv{slot}", ("KV", kv, ti.b, ti.hk, ti.kb0 + blk))
+        st["fill"] += 1
+
+    k = 0
+    while st["alive"]:
+        ok, ti = yield from ring_fetch(sim, k)
+        if not ok or ti is None:
             break
-        if ti.n == 0:
-            continue
+        k += 1
+        if ti.n > 0:
+            yield from load(0, ti, 0)
         for j in range(ti.n):
-            if not alive:
+            if not st["alive"]:
                 break
-            for kv in range(2):
-                slot = kv_fill % S
-                if kv_fill >= S:
-                    ok = yield ("wait", f"kv_empty{slot}", kv_fill // S - 1)
-                    if not ok:
-                        alive = False
-                        break
-                yield ("expect_tx", f"kv_full{slot}", 1)
-                yield ("tma", f"kv_full{slot}", 1, f"kv{slot}", ("KV", kv, ti.b, ti.hk, ti.kb0 + j))
-                kv_fill += 1
+            yield from load(1, ti, j)
+            if st["alive"] and j + 1 < ti.n:
+                yield from load(0, ti, j + 1)
+    kv_fill = st["fill"]
     for s in range(S):
         if kv_fill > s:
             last = s + S * ((kv_fill - 1 - s) // S)
@@ -274,11 +349,62 @@ def _rotate(sim: Sim, buf: int, half: int):
 
 
 def role_qload(sim: Sim, tiles):
-    """Q producer (warp 10); in the rotary variant it also rotates rows 0-63."""
+    """Q producer (warp 10) and producer of the tile ring: entries are handed
+    out in order with one more entry always published ahead of the tile whose
+    Q this warp loads (next_entry / next_work of the kernel); in the rotary
+    variant it also rotates rows 0-63."""
     p = sim.p
     uses = [0] * p.q_bufs
     nq = 0
-    work = [t for t in tiles if t.n > 0]
+    entries = ring_entries(tiles)
+    st = {"produced": 0, "pend": 2, "pend_t": None, "clc": 0, "drained": False}
+
+    def produce():
+        k = st["produced"]
+        if k >= 1 and not st["drained"]:
+            # the next tile index comes from a cluster-launch-control request
+            # (or its failure: no CTA left), completing on the clc barrier
+            slot = k % p.tile_slots
+            if k >= p.tile_slots:
+                ok = yield ("wait", f"tile_empty{slot}", k // p.tile_slots - 1)
+                if not ok:
+                    return -1, None
+            yield ("expect_tx", "clc", 1)
+            yield ("tma", "clc", 1, "clc_resp", ("CLC", st["clc"]))
+            ok = yield ("wait", "clc", st["clc"])
+            if not ok:
+                return -1, None
+
+            def read(n=st["clc"]):
+                sim.expect("clc_resp", ("CLC", n), "launch-control response")
+            yield ("act", read)
+            st["clc"] += 1
+            if entries[k] is None:
+                st["drained"] = True
+            ok = yield from ring_produce(sim, k, entries[k], waited=True)
+        else:
+            ok = yield from ring_produce(sim, k, entries[k])
+        if not ok:
+            return -1, None
+        st["produced"] += 1
+        return (1 if entries[k] is not None else 0), entries[k]
+
+    def next_entry():
+        if st["pend"] == 2:
+            r, t = yield from produce()
+        else:
+            r, t = st["pend"], st["pend_t"]
+        if r > 0:
+            st["pend"], st["pend_t"] = yield from produce()
+        else:
+            st["pend"] = 2
+        return r, t
+
+    def next_work():
+        while True:
+            r, t = yield from next_entry()
+            if not (r > 0 and t.n == 0):
+                return r, t
 
     def load(buf, ti, t):
         if uses[buf] > 0:
@@ -299,23 +425,26 @@ def role_qload(sim: Sim, tiles):
         return True
 
     if not p.rope:
-        for ti in work:
-            if not (yield from load(nq & 1, ti, 0)):
+        while True:
+            r, ti = yield from next_work()
+            if r <= 0:
                 break
-            if not (yield from load(2 + nq % p.q1_bufs, ti, 1)):
+            if not (yield from load(nq & 1, ti, 0)) or not (yield from load(2 + nq % p.q1_bufs, ti, 1)):
                 break
             nq += 1
     else:
-        idx = 0
-        have = bool(work) and (yield from load(0, work[0], 0))
+        r, ti = yield from next_work()
+        have = r > 0 and (yield from load(0, ti, 0))
         lower_rotated = False
         while have:
-            ti = work[idx]
             b0, b1 = nq & 1, 2 + nq % p.q1_bufs
             if not (yield from load(b1, ti, 1)):
                 break
-            more = idx + 1 < len(work)
-            if more and not (yield from load((nq + 1) & 1, work[idx + 1], 0)):
+            rn, tn = yield from next_work()
+            if rn < 0:
+                break
+            more = rn > 0
+            if more and not (yield from load((nq + 1) & 1, tn, 0)):
                 break
             if not lower_rotated and not (yield from rotate(b0, nq >> 1)):
                 break
@@ -325,7 +454,7 @@ def role_qload(sim: Sim, tiles):
                 break
             lower_rotated = True
             nq += 1
-            idx += 1
+            ti = tn
             have = more
     for b in range(p.q_bufs):
         if uses[b] > 0:
@@ -336,7 +465,14 @@ def role_rope_q(sim: Sim, tiles):
     """Rotary variant, warp 11: rotates rows 64-127 of every Q sub-tile."""
     p = sim.p
     nq = 0
-    for ti in [t for t in tiles if t.n > 0]:
+    k = 0
+    while True:
+        ok, ti = yield from ring_fetch(sim, k)
+        if not ok or ti is None:
+            return
+        k += 1
+        if ti.n == 0:
+            continue
         bufs = (nq & 1, 2 + nq % p.q1_bufs)
         uses = (nq >> 1, nq // p.q1_bufs)
         for t in range(2):
@@ -418,11 +554,14 @@ def role_mma(sim: Sim, tiles):
 
     if p.debug_stall:
         alive = yield ("wait", "stall", 0)
-    for ti in tiles:
-        if not alive:
+    k = 0
+    while alive:
+        ok, ti = yield from ring_fetch(sim, k)
+        if not ok or ti is None:
             break
+        k += 1
         n, n0, n1 = ti.n, ti.nb[0], ti.nb[1]
-        if n == 0:
+        if n == 0:                  # no key block: nothing to issue
             continue
         q_buf = (nq & 1, 2 + nq % p.q1_bufs)
         ok = yield ("wait", f"{q_ready}{q_buf[0]}", nq >> 1)
@@ -496,7 +635,12 @@ def role_softmax(sim: Sim, tiles, t: int):
     """Softmax warpgroup t: per block, S_t -> P_t (rescaling O_t), then the epilogue."""
     s_cnt = 0
     o_cnt = 0
-    for ti in tiles:
+    k = 0
+    while True:
+        ok, ti = yield from ring_fetch(sim, k, arrivals=4)     # each of the four warps frees the entry
+        if not ok or ti is None:
+            return
+        k += 1
         nb = ti.nb[t]
         key = _tile_key(ti)
         if nb == 0:
@@ -538,6 +682,10 @@ def make_sim(p: Params, seed: int, timeouts: bool = False):
     for base, n, count in names:
         for i in range(n):
             sim.bars[f"{base}{i}"] = Barrier(f"{base}{i}", count)
+    for i in range(p.tile_slots):
+        sim.bars[f"tile_full{i}"] = Barrier(f"tile_full{i}", 1)
+        sim.bars[f"tile_empty{i}"] = Barrier(f"tile_empty{i}", p.tile_consumers)
+    sim.bars["clc"] = Barrier("clc", 1)
     sim.bars["drain"] = Barrier("drain", 1)
     sim.bars["stall"] = Barrier("stall", 1)
     tiles = schedule(p)

@@ -36,6 +36,11 @@ CASES = [
     M.Params(rope=True, B=2, Hq=2, Hkv=1, Sq=700, Sk=700, grid=2, cta=1),
     M.Params(Sq=128, Sk=128, Hq=1, Hkv=1),                             # one block per tile
     M.Params(Sq=256, Sk=256, Hq=3, Hkv=3, causal=False),
+    # tiles taken over from CTAs that had not started (cluster launch control)
+    M.Params(B=2, Hq=4, Hkv=2, Sq=1200, Sk=1200, cta=3, steal_seed=1),
+    M.Params(B=2, Hq=4, Hkv=2, Sq=1000, Sk=300, cta=0, steal_seed=2, D=64),
+    M.Params(rope=True, B=2, Hq=2, Hkv=1, Sq=900, Sk=900, cta=1, steal_seed=3),
+    M.Params(num_splits=3, Hq=4, Hkv=1, pack_shift=2, Sq=16, Sk=1500, cta=0, steal_seed=4),
 ]
 
 SEEDS = range(12)
@@ -43,7 +48,7 @@ SEEDS = range(12)
 
 def _id(p):
     return f"D{p.D}_c{int(p.causal)}_B{p.B}H{p.Hq}-{p.Hkv}_S{p.Sq}-{p.Sk}_sp{p.num_splits}_r{int(p.rope)}" \
-           f"_pk{p.pack_shift}_g{p.grid}.{p.cta}"
+           f"_pk{p.pack_shift}_g{p.grid}.{p.cta}_st{p.steal_seed}"
 
 
 @pytest.mark.parametrize("p", CASES, ids=_id)
@@ -53,7 +58,7 @@ def test_protocol_has_no_deadlock_or_race(p):
         M.run(p, seed=seed, bias=(seed % 4) / 4)
 
 
-@pytest.mark.parametrize("p", [CASES[0], CASES[1], CASES[7], CASES[10]], ids=_id)
+@pytest.mark.parametrize("p", [CASES[0], CASES[1], CASES[7], CASES[10], CASES[15]], ids=_id)
 def test_stalled_wait_aborts_every_role(p):
     """The stall hook: the MMA issuer waits on a barrier nothing signals; its
     wait runs out, and every role must then finish, shutdown waits included."""
@@ -63,7 +68,7 @@ def test_stalled_wait_aborts_every_role(p):
         assert sim.timed_out
 
 
-@pytest.mark.parametrize("p", [CASES[0], CASES[2], CASES[5], CASES[11]], ids=_id)
+@pytest.mark.parametrize("p", [CASES[0], CASES[2], CASES[5], CASES[11], CASES[16]], ids=_id)
 def test_abort_at_any_moment_terminates(p):
     """Some wait runs out at an arbitrary step: no role may hang afterwards."""
     total = M.run(p, seed=0).steps
@@ -78,12 +83,12 @@ MUTATIONS = {
     # the MMA issuer never releases a ring slot after the V products
     "kv_empty_commit_dropped": ('            yield ("commit", f"kv_empty{vs}")\n', ""),
     # the producer waits for the slot's current phase instead of the previous one
-    "ring_wait_wrong_phase": ('ok = yield ("wait", f"kv_empty{slot}", kv_fill // S - 1)',
-                              'ok = yield ("wait", f"kv_empty{slot}", kv_fill // S)'),
+    "ring_wait_wrong_phase": ('ok = yield ("wait", f"kv_empty{slot}", st["fill"] // S - 1)',
+                              'ok = yield ("wait", f"kv_empty{slot}", st["fill"] // S)'),
     # the producer reuses a slot without waiting for its release
-    "ring_wait_skipped": ("                if kv_fill >= S:\n", "                if False:\n"),
+    "ring_wait_skipped": ('        if st["fill"] >= S:\n', "        if False:\n"),
     # V before K in the ring: the issuer takes the wrong tiles
-    "ring_order_swapped": ('("KV", kv, ti.b, ti.hk, ti.kb0 + j)', '("KV", 1 - kv, ti.b, ti.hk, ti.kb0 + j)'),
+    "ring_order_swapped": ('("KV", kv, ti.b, ti.hk, ti.kb0 + blk)', '("KV", 1 - kv, ti.b, ti.hk, ti.kb0 + blk)'),
     # Q buffers released one block early
     "q_release_early": ("                if j + 1 == n - 1:\n", "                if j + 2 == n - 1 or (n == 2 and j == 0):\n"),
     # the next S_t written before P_t has been consumed
@@ -133,11 +138,18 @@ MUTATIONS = {
     # the issuer waits for Q of the upper sub-tile on the lower sub-tile's buffer
     "q_buffer_mixup": ('ok = yield ("wait", f"{q_ready}{q_buf[1]}", nq // p.q1_bufs)',
                        'ok = yield ("wait", f"{q_ready}{q_buf[0]}", nq >> 1)'),
+    # the tile-ring producer overwrites entries without waiting for them to be freed
+    "ring_producer_skips_wait": ("    if k >= p.tile_slots:\n", "    if False:\n"),
+    # one arrival too few frees a tile-ring entry (a consumer not counted)
+    "ring_consumer_undercount": ("        return 1 + 1 + 8 + (1 if self.rope else 0)", "        return 1 + 8 + (1 if self.rope else 0)"),
+    # the producer reads the launch-control response without waiting for it
+    "clc_wait_skipped": ('            ok = yield ("wait", "clc", st["clc"])', '            ok = True'),
     # the K/V producer stops draining its copies on shutdown
     "drain_skipped": ('            yield ("drain", f"kv_full{s}", last // S)', "            pass"),
 }
 
-MUTATION_CASES = [CASES[0], CASES[1], CASES[2], CASES[5], CASES[7], CASES[10], CASES[12]]
+MUTATION_CASES = [CASES[0], CASES[1], CASES[2], CASES[5], CASES[7], CASES[10], CASES[12], CASES[15],
+                  M.Params(B=2, Hq=4, Hkv=2, Sq=1200, Sk=1200, grid=1, tile_slots=2)]
 
 
 def _mutant(name):
@@ -170,6 +182,7 @@ def test_planted_protocol_bug_is_caught(name):
         q = mod.Params(**p.__dict__)
         total = M.run(p, seed=0).steps
         for seed in SEEDS:
-            if _caught(mod, p=q, seed=seed, timeouts=True, abort_at=max(2, int(total * (seed + 1) / 14))):
-                return
+            for frac in (0.1, 0.3, 0.5, 0.7, 0.9):
+                if _caught(mod, p=q, seed=seed, timeouts=True, abort_at=max(2, int(total * frac))):
+                    return
     pytest.fail(f"planted protocol bug {name!r} was not detected")

@@ -497,7 +497,11 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     p.rope = rope ? rope->table : nullptr;
     p.q_pos0 = rope ? rope->q_pos0 : 0;
 
-    const int grid = p.n_tiles < dev->num_sms ? p.n_tiles : dev->num_sms;
+    // One CTA per work tile. At most one CTA fits on an SM; the running CTAs
+    // take over the tiles of CTAs that have not started yet (cluster launch
+    // control), so the grid behaves as a persistent one with a dynamic,
+    // longest-first schedule.
+    const int grid = p.n_tiles;
     if (rope)
         rc = bf16 ? launch_any<true, true, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
                   : launch_any<false, true, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);

@@ -78,13 +78,17 @@ constexpr int kRopeWarp = 11;               // second rotating warp of the rotar
 // 128 x (200 + 200 + 104) = 64512. The host refuses to launch unless the
 // compiled kernel uses exactly kLaunchRegs, so the split always fits.
 constexpr int kLaunchRegs = 168;
-constexpr uint32_t kSoftmaxRegs = 200;
-constexpr uint32_t kControlRegs = 104;
+constexpr uint32_t kSoftmaxRegs = 192;
+constexpr uint32_t kControlRegs = 120;
 static_assert(128 * (2 * kSoftmaxRegs + kControlRegs) <= kThreads * kLaunchRegs, "register split");
 constexpr int kBlockM = 128;        // query rows per softmax warpgroup
 constexpr int kBlockN = 128;        // keys per K/V tile
 constexpr int kRowsPerTile = 2 * kBlockM;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
+constexpr int kTileSlots = 8;               // entries of the shared-memory tile ring
+// Arrivals that free a tile-ring entry: the K/V producer, the MMA issuer, the
+// eight softmax warps and, in the rotary variant, warp 11.
+__host__ __device__ constexpr uint32_t tile_consumers(bool rope) { return 1 + 1 + 8 + (rope ? 1u : 0u); }
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 constexpr unsigned int kStatusTimeout = 1u;
 
@@ -114,8 +118,14 @@ struct TileCfg {
     static constexpr int bKVFull = bStall + 1;        // [kSlots]
     static constexpr int bKVEmpty = bKVFull + kSlots;
     static constexpr int bQRdy = bKVEmpty + kSlots;   // [kQBufs] rotary variant: Q rotated (two arrivals)
-    static constexpr int kNumBars = bQRdy + kQBufs;
-    static constexpr int kTmemSlotOff = kBarOff + 8 * kNumBars;
+    static constexpr int bTileFull = bQRdy + kQBufs;  // [kTileSlots] tile ring entry published
+    static constexpr int bTileEmpty = bTileFull + kTileSlots;   // [kTileSlots] entry freed by every consumer
+    static constexpr int bClc = bTileEmpty + kTileSlots;      // cluster-launch-control response landed
+    static constexpr int kNumBars = bClc + 1;
+    // tile ring: kTileSlots entries of 32 bytes, read and written as 16-byte vectors
+    static constexpr int kTileOff = (kBarOff + 8 * kNumBars + 31) / 32 * 32;
+    static constexpr int kClcOff = kTileOff + kTileSlots * 32;   // 16-byte cluster-launch-control response
+    static constexpr int kTmemSlotOff = kClcOff + 16;
     static constexpr int kAbortOff = kTmemSlotOff + 4;
     static constexpr int kSmemUsed = kAbortOff + 4;
     static constexpr int kSmemBytes = kSmemUsed + 1024;       // + alignment slack
@@ -124,6 +134,10 @@ struct TileCfg {
     static constexpr int kOCol0 = 256;
     static_assert(kOCol0 + 2 * D <= 512, "TMEM budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
+    static_assert(kKVOff % 1024 == 0 && kBarOff % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+    static_assert(kTileOff % 32 == 0, "tile ring entries are accessed as 16-byte vectors");
+    static_assert(kClcOff % 16 == 0, "the launch-control response is a 16-byte value");
+    static_assert(kTmemSlotOff % 4 == 0 && kAbortOff % 4 == 0, "4-byte words");
 };
 
 struct TileInfo {
@@ -176,14 +190,6 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const FwdParams& p) {
     return t;
 }
 
-// Persistent schedule: wave w hands CTA c the tile w*G + c for even w and
-// w*G + G-1-c for odd w (G = grid size). Walking the longest-first list in
-// this back-and-forth order pairs long tiles with short ones on each CTA.
-__device__ __forceinline__ int tile_of_wave(int w) {
-    const int G = gridDim.x;
-    return w * G + ((w & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
-}
-
 struct SyncCtx {
     volatile uint32_t* abort_flag;
     unsigned int* status;
@@ -225,41 +231,84 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const S
     return __all_sync(0xffffffffu, wait_phase(bar, parity, sc));
 }
 
+// ------------------------------------------------------------- tile ring
+// The Q warp computes each work tile once (tile_info's integer divisions stay
+// off every other role's path, the MMA issuer's above all) and publishes it in
+// a ring of kTileSlots shared-memory entries of 32 bytes: tile_full[slot]
+// completes when the entry is written; every consumer (the K/V producer, the
+// MMA issuer, each softmax warp and, in the rotary variant, warp 11) copies the
+// entry and frees it at once with one arrival on tile_empty[slot]. After the
+// last tile the producer publishes an end marker (nb = -1).
+__device__ __forceinline__ void store_tile_entry(uint8_t* entry, const TileInfo& t) {
+    int4* e = reinterpret_cast<int4*>(entry);
+    e[0] = make_int4(t.b, t.h, t.hk, t.m0);
+    e[1] = make_int4(t.split, t.kb0, t.nb[0], t.nb[1]);
+}
+
+__device__ __forceinline__ TileInfo load_tile_entry(const uint8_t* entry) {
+    const int4* e = reinterpret_cast<const int4*>(entry);
+    const int4 a = e[0], c = e[1];
+    TileInfo t;
+    t.b = a.x;
+    t.h = a.y;
+    t.hk = a.z;
+    t.m0 = a.w;
+    t.split = c.x;
+    t.kb0 = c.y;
+    t.nb[0] = c.z;
+    t.nb[1] = c.w;
+    t.n = max(c.z, c.w);
+    return t;
+}
+
+// A warp copies entry k of the tile ring and frees it (one arrival, lane 0).
+// Returns false when the wait was aborted; t.n < 0 marks the end of the work.
+__device__ __forceinline__ bool fetch_tile_warp(uint32_t full_bar, uint32_t empty_bar, const uint8_t* ring, uint32_t k,
+                                                TileInfo& t, const SyncCtx& sc) {
+    const uint32_t slot = k % kTileSlots;
+    if (!warp_wait(full_bar + 8u * slot, (k / kTileSlots) & 1u, sc)) return false;
+    t = load_tile_entry(ring + 32 * slot);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(empty_bar + 8u * slot);
+    return true;
+}
+
 // ------------------------------------------------------------ TMA producer
 // The whole warp runs this loop (so that addresses and coordinates stay
-// warp-uniform); lane 0 issues the copies.
-template <int D, bool CAUSAL, bool PACK>
-__device__ void role_tma(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
-                         const FwdParams& p, uint32_t smem, const SyncCtx& sc) {
+// warp-uniform); lane 0 issues the copies. The K/V tiles enter the ring in the
+// order the MMA issuer takes them: K_0, then per block V_j and K_{j+1}. The
+// work tiles come from the tile ring.
+template <int D>
+__device__ void role_tma(const CUtensorMap* tmK, const CUtensorMap* tmV, uint32_t smem, const uint8_t* smem_ptr,
+                         const SyncCtx& sc) {
     using C = TileCfg<D>;
     const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     uint32_t kv_fill = 0;
+    auto load = [&](const CUtensorMap* map, const TileInfo& t, int blk) -> bool {
+        const uint32_t slot = kv_fill % C::kSlots;
+        if (kv_fill >= (uint32_t)C::kSlots &&
+            !warp_wait(bar(C::bKVEmpty + slot), ((kv_fill / C::kSlots) - 1) & 1u, sc))
+            return false;
+        if (leader) {
+            ptx::mbar_arrive_expect_tx(bar(C::bKVFull + slot), C::kTileBytes);
+            for (int c = 0; c < C::kBoxes; ++c)
+                ptx::tma_load_4d(smem + C::kKVOff + slot * C::kTileBytes + c * C::kBoxBytes, map,
+                                 bar(C::bKVFull + slot), c * C::kBoxCols, t.hk, (t.kb0 + blk) * kBlockN, t.b);
+        }
+        ++kv_fill;
+        return true;
+    };
+    const uint8_t* ring = smem_ptr + C::kTileOff;
     bool alive = true;
-    for (int w = 0; w * (int)gridDim.x < p.n_tiles && alive; ++w) {
-        const int tile = tile_of_wave(w);
-        if (tile >= p.n_tiles) continue;
-        const TileInfo ti = tile_info<CAUSAL, PACK>(tile, p);
-        if (ti.n == 0) continue;
+    for (uint32_t k = 0; alive; ++k) {
+        TileInfo ti;
+        if (!fetch_tile_warp(bar(C::bTileFull), bar(C::bTileEmpty), ring, k, ti, sc) || ti.n < 0) break;
+        if (ti.n > 0) alive = load(tmK, ti, 0);
         for (int j = 0; j < ti.n && alive; ++j) {
-            for (int kv = 0; kv < 2; ++kv) {
-                const uint32_t slot = kv_fill % C::kSlots;
-                if (kv_fill >= (uint32_t)C::kSlots &&
-                    !warp_wait(bar(C::bKVEmpty + slot), ((kv_fill / C::kSlots) - 1) & 1u, sc)) {
-                    alive = false;
-                    break;
-                }
-                if (leader) {
-                    ptx::mbar_arrive_expect_tx(bar(C::bKVFull + slot), C::kTileBytes);
-                    const CUtensorMap* map = kv ? tmV : tmK;
-                    for (int c = 0; c < C::kBoxes; ++c)
-                        ptx::tma_load_4d(smem + C::kKVOff + slot * C::kTileBytes + c * C::kBoxBytes, map,
-                                         bar(C::bKVFull + slot), c * C::kBoxCols, ti.hk, (ti.kb0 + j) * kBlockN,
-                                         ti.b);
-                }
-                ++kv_fill;
-            }
+            alive = load(tmV, ti, j);
+            if (alive && j + 1 < ti.n) alive = load(tmK, ti, j + 1);
         }
     }
     // Shut down: wait until every copy this warp started has landed.
@@ -344,33 +393,21 @@ __device__ __forceinline__ void rope_rotate_rows(uint8_t* tile, int r_begin, int
     __syncwarp();
 }
 
-// Next work tile with at least one key block, from wave w0 on.
-template <bool CAUSAL, bool PACK = false>
-__device__ bool next_work_tile(const FwdParams& p, int w0, int& w_out, TileInfo& t_out) {
-    for (int w = w0; w * (int)gridDim.x < p.n_tiles; ++w) {
-        const int tile = tile_of_wave(w);
-        if (tile >= p.n_tiles) continue;
-        t_out = tile_info<CAUSAL, PACK>(tile, p);
-        if (t_out.n == 0) continue;
-        w_out = w;
-        return true;
-    }
-    return false;
-}
-
 // Rotary variant, warp 11: rotates rows 64..127 of every Q sub-tile once its
 // load has landed (the Q warp does rows 0..63), in the order the Q warp loads
 // them, and signals "Q ready" (two arrivals per use).
-template <int D, bool CAUSAL, bool BF16>
+template <int D, bool BF16>
 __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr, const SyncCtx& sc) {
     using C = TileCfg<D>;
     const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    const uint8_t* ring = smem_ptr + C::kTileOff;
     uint32_t nq = 0;
-    int w = -1;
-    TileInfo ti;
-    while (next_work_tile<CAUSAL>(p, w + 1, w, ti)) {
+    for (uint32_t k = 0;; ++k) {
+        TileInfo ti;
+        if (!fetch_tile_warp(bar(C::bTileFull), bar(C::bTileEmpty), ring, k, ti, sc) || ti.n < 0) return;
+        if (ti.n == 0) continue;
         const int buf[2] = {(int)(nq & 1u), 2 + (int)(nq % C::kQ1Bufs)};
         const uint32_t use[2] = {nq >> 1, nq / C::kQ1Bufs};
         for (int t = 0; t < 2; ++t) {
@@ -384,11 +421,14 @@ __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr
 }
 
 // ------------------------------------------------------------- Q producer
-// Loads the Q sub-tiles of each work tile. The lower sub-tile alternates
-// between two buffers, so it is fetched as soon as the tile before the current
-// one has finished with it; the upper sub-tile reuses one buffer and is fetched
-// while the previous tile's last products and epilogue run. In the rotary
-// variant this warp also rotates rows 0..63 of each sub-tile after it lands.
+// Produces the tile ring and loads the Q sub-tiles of each work tile. Each
+// entry is published one entry ahead of the tile whose Q this warp loads, so
+// that the roles that peek at the next tile (K/V producer, MMA issuer) never
+// wait on this warp's own Q waits. The lower sub-tile alternates between two
+// buffers, so it is fetched as soon as the tile before the current one has
+// finished with it; the upper sub-tile reuses one buffer and is fetched while
+// the previous tile's last products and epilogue run. In the rotary variant
+// this warp also rotates rows 0..63 of each sub-tile after it lands.
 template <int D, bool CAUSAL, bool BF16, bool ROPE, bool PACK>
 __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t smem, uint8_t* smem_ptr,
                            const SyncCtx& sc) {
@@ -396,6 +436,82 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
     const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
+    uint8_t* ring = smem_ptr + C::kTileOff;
+    // ---- tile ring producer: this CTA's own tile, then the tiles of CTAs that
+    // had not started yet (taken over through cluster launch control), then
+    // the end marker.
+    uint32_t produced = 0;
+    uint32_t clc_uses = 0;
+    bool own = true, drained = false;
+    // Index of the next tile for this CTA: 1 (tile set), 0 (none left), -1 (aborted).
+    auto next_tile_index = [&](int& tile) -> int {
+        if (own) {
+            own = false;
+            tile = (int)blockIdx.x;
+            return 1;
+        }
+        if (drained) return 0;
+        const uint32_t resp = smem + C::kClcOff;
+        if (leader) {
+            ptx::mbar_arrive_expect_tx(bar(C::bClc), 16);
+            ptx::clc_try_cancel(resp, bar(C::bClc));
+        }
+        if (!warp_wait(bar(C::bClc), clc_uses & 1u, sc)) return -1;
+        ++clc_uses;
+        uint32_t x = 0;
+        const bool got = ptx::clc_query(resp, x);
+        __syncwarp();                              // every lane has read the response
+        if (!got || x >= (uint32_t)p.n_tiles) {
+            drained = true;                        // no CTA left to take over
+            return 0;
+        }
+        tile = (int)x;
+        return 1;
+    };
+    // Publishes the next entry. Returns 1 (t = the tile), 0 (end marker) or -1 (aborted).
+    auto produce = [&](TileInfo& t) -> int {
+        const uint32_t slot = produced % kTileSlots;
+        if (produced >= (uint32_t)kTileSlots &&
+            !warp_wait(bar(C::bTileEmpty + slot), ((produced / kTileSlots) - 1) & 1u, sc))
+            return -1;
+        int tile = 0;
+        const int found = next_tile_index(tile);
+        if (found < 0) return -1;
+        if (found) t = tile_info<CAUSAL, PACK>(tile, p);
+        if (!found) {
+            t.b = t.h = t.hk = t.m0 = t.split = t.kb0 = 0;
+            t.nb[0] = t.nb[1] = t.n = -1;
+        }
+        if (leader) {
+            store_tile_entry(ring + 32 * slot, t);
+            ptx::mbar_arrive(bar(C::bTileFull + slot));
+        }
+        ++produced;
+        return found;
+    };
+    TileInfo pend;
+    int pend_state = 2;                         // 2: nothing published ahead
+    // The next entry in order, keeping one more entry published ahead of it.
+    auto next_entry = [&](TileInfo& t) -> int {
+        int r;
+        if (pend_state == 2) {
+            r = produce(t);
+        } else {
+            t = pend;
+            r = pend_state;
+        }
+        pend_state = r > 0 ? produce(pend) : 2;
+        return r;
+    };
+    // The next tile with at least one key block (1), the end (0) or an abort (-1).
+    auto next_work = [&](TileInfo& t) -> int {
+        int r;
+        do {
+            r = next_entry(t);
+        } while (r > 0 && t.n == 0);
+        return r;
+    };
+
     uint32_t uses[C::kQBufs] = {};              // loads issued into each buffer
     uint32_t nq = 0;                            // work tiles with at least one block
     auto load = [&](int buf, int row0, const TileInfo& ti) -> bool {
@@ -416,11 +532,8 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
         return true;
     };
     if (!ROPE) {
-        for (int w = 0; w * (int)gridDim.x < p.n_tiles; ++w) {
-            const int tile = tile_of_wave(w);
-            if (tile >= p.n_tiles) continue;
-            const TileInfo ti = tile_info<CAUSAL, PACK>(tile, p);
-            if (ti.n == 0) continue;
+        TileInfo ti;
+        while (next_work(ti) > 0) {
             if (!load(nq & 1, ti.m0, ti) || !load(2 + nq % C::kQ1Bufs, ti.m0 + (kBlockM >> (PACK ? p.pack_shift : 0)), ti))
                 break;
             ++nq;
@@ -431,23 +544,21 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
         // right after it); rotations follow in load order: the upper sub-tile
         // of T as soon as it lands, then the next tile's lower one, which
         // therefore is ready a whole tile ahead.
-        int w = 0;
-        TileInfo ti;
-        bool have = next_work_tile<CAUSAL>(p, 0, w, ti) && load(0, ti.m0, ti);
+        TileInfo ti, tn;
+        bool have = next_work(ti) > 0 && load(0, ti.m0, ti);
         bool lower_rotated = false;
         while (have) {
             const int b0 = nq & 1, b1 = 2 + nq % C::kQ1Bufs;
             if (!load(b1, ti.m0 + kBlockM, ti)) break;
-            int w_next = 0;
-            TileInfo tn;
-            const bool more = next_work_tile<CAUSAL>(p, w + 1, w_next, tn);
+            const int rn = next_work(tn);
+            if (rn < 0) break;
+            const bool more = rn > 0;
             if (more && !load((nq + 1) & 1, tn.m0, tn)) break;
             if (!lower_rotated && !rotate(b0, nq >> 1, ti.m0)) break;
             if (!rotate(b1, nq / C::kQ1Bufs, ti.m0 + kBlockM)) break;
             if (more && !rotate((nq + 1) & 1, (nq + 1) >> 1, tn.m0)) break;
             lower_rotated = true;
             ++nq;
-            w = w_next;
             ti = tn;
             have = more;
         }
@@ -475,8 +586,8 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
 // two groups of MMAs can leave it idle. For the same reason the next K/V slot
 // is probed (without blocking) before a group is issued, and the wait after
 // the group is skipped when the probe already saw the slot full.
-template <int D, bool CAUSAL, bool BF16, bool ROPE, bool PACK>
-__device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const SyncCtx& sc) {
+template <int D, bool BF16, bool ROPE>
+__device__ void role_mma(const FwdParams& p, uint32_t smem, const uint8_t* smem_ptr, uint32_t tmem, const SyncCtx& sc) {
     using C = TileCfg<D>;
     const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
@@ -508,8 +619,9 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
     auto commit = [&](int b) {
         if (leader) ptx::tc_commit(bar(b));
     };
-    auto issue_qk = [&](int t, uint32_t k_slot) {
-        const uint64_t qd = q_desc0 + (uint64_t)((q_buf[t] * C::kTileBytes) >> 4);
+    // S_t = Q K^T from Q buffer qb and the K tile in ring slot k_slot.
+    auto issue_qk = [&](int t, uint32_t qb, uint32_t k_slot) {
+        const uint64_t qd = q_desc0 + (uint64_t)((qb * C::kTileBytes) >> 4);
         const uint64_t kd = kv_desc0 + (uint64_t)((k_slot * C::kTileBytes) >> 4);
         if (leader) {
 #pragma unroll
@@ -539,12 +651,22 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
 
     if (!leader) return;
     if (p.debug_stall) alive = wait_phase(bar(C::bStall), 0, sc);   // nothing ever arrives
-    for (int w = 0; w * (int)gridDim.x < p.n_tiles && alive; ++w) {
-        const int tile = tile_of_wave(w);
-        if (tile >= p.n_tiles) continue;
-        const TileInfo ti = tile_info<CAUSAL, PACK>(tile, p);
-        const int n = ti.n, n0 = ti.nb[0], n1 = ti.nb[1];     // n0, n1 are n or n - 1
-        if (n == 0) continue;
+    // Sizes of tile-ring entry k (the issuer reads only the block counts).
+    const uint8_t* ring = smem_ptr + C::kTileOff;
+    auto fetch = [&](uint32_t k, int& nb0, int& nb1) -> bool {
+        const uint32_t slot = k % kTileSlots;
+        if (!wait_phase(bar(C::bTileFull + slot), (k / kTileSlots) & 1u, sc)) return false;
+        const int4 c = reinterpret_cast<const int4*>(ring + 32 * slot)[1];
+        nb0 = c.z;
+        nb1 = c.w;
+        ptx::mbar_arrive(bar(C::bTileEmpty + slot));
+        return true;
+    };
+    for (uint32_t k = 0; alive; ++k) {
+        int n0 = 0, n1 = 0;             // block counts of the tile's sub-tiles
+        if (!fetch(k, n0, n1) || n1 < 0) break;      // n1 < 0: end marker
+        const int n = max(n0, n1);      // n0, n1 are n or n - 1
+        if (n == 0) continue;           // no key block for any row: nothing to issue
         // Q buffers of this tile: lower sub-tile in buffer nq & 1 (its (nq >> 1)-th
         // use), upper sub-tile in buffer 2 (its nq-th use). Both phases are consumed
         // even when a sub-tile has no block, to keep the parities in step.
@@ -556,12 +678,12 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
         };
         uint32_t ks, vs;
         if (!wait_phase(bar(kQReady + q_buf[0]), (nq >> 1) & 1u, sc) || !acquire(ks)) { alive = false; break; }
-        if (n0 > 0) issue_qk(0, ks);
+        if (n0 > 0) issue_qk(0, q_buf[0], ks);
         issued = true;
         if (!wait_phase(bar(kQReady + q_buf[1]), (nq / C::kQ1Bufs) & 1u, sc)) { alive = false; break; }
         ptx::tc_fence_after_sync();
         ++nq;
-        if (n1 > 0) issue_qk(1, ks);
+        if (n1 > 0) issue_qk(1, q_buf[1], ks);
         commit(C::bKVEmpty + ks);
         if (n == 1) release_q();
         bool v_seen = false;
@@ -576,7 +698,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
             }
             if (more) {
                 if (!acquire(ks, k_seen)) { alive = false; break; }
-                if (j + 1 < n0) issue_qk(0, ks);
+                if (j + 1 < n0) issue_qk(0, q_buf[0], ks);
             }
             if (j < n1) {
                 if (!wait_p(1)) { alive = false; break; }
@@ -586,7 +708,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
             commit(C::bKVEmpty + vs);
             if (more) {
                 v_seen = probe_next();
-                if (j + 1 < n1) issue_qk(1, ks);
+                if (j + 1 < n1) issue_qk(1, q_buf[1], ks);
                 commit(C::bKVEmpty + ks);
                 if (j + 1 == n - 1) release_q();
             }
@@ -601,7 +723,8 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, uint32_t tmem, const
 
 // ------------------------------------------------ softmax / epilogue warpgroup
 template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool PACK>
-__device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, int wg, const SyncCtx& sc) {
+__device__ void role_softmax(const FwdParams& p, uint32_t smem, const uint8_t* smem_ptr, uint32_t tmem, int wg,
+                             const SyncCtx& sc) {
     using C = TileCfg<D>;
     const uint32_t bars = smem + C::kBarOff;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
@@ -614,10 +737,11 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint32_t tmem, i
     constexpr float kLog2e = 1.4426950408889634f;
     uint32_t s_phase = 0, o_phase = 0;
 
-    for (int w = 0; w * (int)gridDim.x < p.n_tiles; ++w) {
-        const int tile = tile_of_wave(w);
-        if (tile >= p.n_tiles) continue;
-        const TileInfo ti = tile_info<CAUSAL, PACK>(tile, p);
+    const uint8_t* ring = smem_ptr + C::kTileOff;
+    for (uint32_t k = 0;; ++k) {
+        TileInfo ti;
+        if (!fetch_tile_warp(bar(C::bTileFull), bar(C::bTileEmpty), ring, k, ti, sc)) return;
+        if (ti.n < 0) break;                                  // end marker
         const int nb = ti.nb[wg];
         const int ps = PACK ? p.pack_shift : 0;
         const int row = ti.m0 + ((wg * kBlockM + r) >> ps);                   // query row
@@ -850,7 +974,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kTmaWarp && lane == 0) {
         const uint32_t bars = smem + C::kBarOff;
         for (int i = 0; i < C::kNumBars; ++i) {
-            ptx::mbar_init(bars + 8u * i, (i >= C::bQRdy && i < C::bQRdy + C::kQBufs) ? 2u : 1u);
+            uint32_t count = 1;
+            if (i >= C::bQRdy && i < C::bQRdy + C::kQBufs) count = 2;
+            if (i >= C::bTileEmpty && i < C::bTileEmpty + kTileSlots) count = tile_consumers(ROPE);
+            ptx::mbar_init(bars + 8u * i, count);
         }
         *abort_flag = 0u;
         ptx::fence_barrier_init();
@@ -871,17 +998,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < 8) {
         ptx::setmaxnreg_inc<kSoftmaxRegs>();
-        role_softmax<D, CAUSAL, ADDITIVE, BF16, PACK>(p, smem, tmem, warp >> 2, sc);
+        role_softmax<D, CAUSAL, ADDITIVE, BF16, PACK>(p, smem, smem_ptr, tmem, warp >> 2, sc);
     } else {
         ptx::setmaxnreg_dec<kControlRegs>();
         if (warp == kMmaWarp)
-            role_mma<D, CAUSAL, BF16, ROPE, PACK>(p, smem, tmem, sc);
+            role_mma<D, BF16, ROPE>(p, smem, smem_ptr, tmem, sc);
         else if (warp == kTmaWarp)
-            role_tma<D, CAUSAL, PACK>(&tmQ, &tmK, &tmV, p, smem, sc);
+            role_tma<D>(&tmK, &tmV, smem, smem_ptr, sc);
         else if (warp == kQWarp)
             role_qload<D, CAUSAL, BF16, ROPE, PACK>(&tmQ, p, smem, smem_ptr, sc);
         else if (ROPE && warp == kRopeWarp)
-            role_rope_q<D, CAUSAL, BF16>(p, smem, smem_ptr, sc);
+            role_rope_q<D, BF16>(p, smem, smem_ptr, sc);
         __syncwarp();
     }
 
