@@ -64,6 +64,7 @@ class Params:
     cta: int = 0                 # which CTA of the grid is modelled
     debug_stall: bool = False    # the MMA issuer first waits on a barrier nothing signals
     tile_slots: int = 8          # entries of the shared-memory tile ring
+    head_group: int = 0          # slices per group of the tile order (0: all slices)
     steal_seed: int = -1         # >= 0: the CTA's tiles are its own and a random set taken over from CTAs
                                  # that had not started (cluster launch control), in launch order
 
@@ -127,14 +128,27 @@ def schedule(p: Params):
         while w * p.grid < n_tiles:
             order.append(w * p.grid + ((p.grid - 1 - p.cta) if (w & 1) else p.cta))
             w += 1
+    slices = p.B * heads
+    head_group = max(1, min(slices, p.head_group or slices))
+    tail_levels = min(2, n_mblk) if p.causal else 0
+    head_levels = n_mblk - tail_levels
+    grouped = slices * head_levels * n_splits
     for tile in order:
         if tile >= n_tiles:
             continue
-        bh_count = p.B * heads
-        per_mb = bh_count * n_splits
-        mb_rank, rem = divmod(tile, per_mb)
-        split, bh = divmod(rem, bh_count)
-        mb = (n_mblk - 1 - mb_rank) if p.causal else mb_rank
+        if tile < grouped:                  # grouped slices, longest query block first
+            per_slice = head_levels * n_splits
+            g0 = tile // (head_group * per_slice) * head_group
+            gs = min(head_group, slices - g0)
+            local = tile - g0 * per_slice
+            level, rem = divmod(local, gs * n_splits)
+            split, r = divmod(rem, gs)
+            bh = g0 + r
+            mb = (n_mblk - 1 - level) if p.causal else level
+        else:                               # the shortest levels of every slice, last
+            level, rem = divmod(tile - grouped, slices * n_splits)
+            split, bh = divmod(rem, slices)
+            mb = (tail_levels - 1 - level) if p.causal else head_levels + level
         b, hh = divmod(bh, heads)
         h = hh * group if ps else hh
         hk = hh if ps else hh // group

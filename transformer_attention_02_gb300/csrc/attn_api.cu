@@ -299,6 +299,9 @@ __global__ void __launch_bounds__(256) rope_apply_kernel(const uint4* x, uint4* 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
 
 constexpr int kMaxSplits = 1024;
+// K/V bytes per group of slices in the tile order: small enough that a group's
+// K/V stays in L2 (about 126 MB on GB300) beside the streamed Q and O.
+constexpr double kOrderGroupKVBytes = 32.0 * (1 << 20);
 constexpr size_t kWorkspaceAlign = 256;
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
@@ -484,14 +487,22 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     p.split_blocks = splits > 1 ? split_blocks : ceil_div(Sk, attn::kBlockN);
     p.n_tiles = (int)(B * tile_heads * n_mblk * splits);
     p.pack_shift = pack_shift;
+    // Tile order (see tile_info): groups of slices holding about
+    // kOrderGroupKVBytes of K/V each.
+    {
+        const long long slices = (long long)B * tile_heads;
+        const long long share = pack_shift ? 1 : Hq / Hkv;         // query-head slices per K/V head
+        const double kv_head_bytes = 4.0 * Sk * D;                 // K and V of one K/V head, 16-bit
+        const long long kv_heads = std::max(1LL, (long long)(kOrderGroupKVBytes / kv_head_bytes));
+        p.head_group = (int)std::max(1LL, std::min(slices, kv_heads * share));
+    }
     if (splits > 1) {
         p.o_part = static_cast<float*>(workspace);
         p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + lse_off);
     }
     p.scale_log2 = scale * 1.4426950408889634f;
     p.mask_vec4 = !additive ? 0 : (aligned(mask, 32) && Sk % 8 == 0) ? 2 : (aligned(mask, 16) && Sk % 4 == 0) ? 1 : 0;
-    p.o_vec8 = aligned(o, 32);
-    p.debug_stall = g_debug_stall.load();
+    p.flags = (aligned(o, 32) ? attn::kFlagOVec8 : 0) | (g_debug_stall.load() ? attn::kFlagDebugStall : 0);
     p.timeout_ns = g_timeout_ns.load();
     p.status = dev->status;
     p.rope = rope ? rope->table : nullptr;

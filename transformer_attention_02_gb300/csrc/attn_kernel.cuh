@@ -57,8 +57,8 @@ struct FwdParams {
     float* lse_part;          // split keys: FP32 LSE of each key range (n_splits, B, Hq, Sq)
     float scale_log2;         // scale * log2(e)
     int mask_vec4;            // mask rows may be read with 32-byte (2) or 16-byte (1) loads, else 0
-    int o_vec8;               // O rows may be written with 32-byte stores
-    int debug_stall;          // wait on a barrier nothing signals (timeout test)
+    int flags;                // kFlagOVec8 | kFlagDebugStall
+    int head_group;           // tile order: (b, head) slices per group (see tile_info)
     unsigned long long timeout_ns;
     unsigned int* status;     // device status word, bit 0 = a wait timed out
     const float* rope;        // rotary table (max_pos, D/2, {cos, sin}) FP32 (rotating variant only)
@@ -67,6 +67,12 @@ struct FwdParams {
     // measurably changed the code generated for the unpacked kernels.
     int pack_shift;           // > 0: the 2^pack_shift query heads of a K/V head share each tile's rows
 };
+// Kept at 128 bytes, with the 64-bit fields where they are: appending two int
+// fields (136 bytes) made the kernel 5% slower on the Llama-2-7B-shaped
+// prefill, with the same code otherwise.
+static_assert(sizeof(FwdParams) <= 128, "FwdParams size");
+constexpr int kFlagOVec8 = 1;         // O rows may be written with 32-byte stores
+constexpr int kFlagDebugStall = 2;    // the MMA issuer waits on a barrier nothing signals (timeout test)
 
 constexpr int kThreads = 384;               // three warpgroups
 constexpr int kMmaWarp = 8;
@@ -148,9 +154,17 @@ struct TileInfo {
     int n;          // max(nb[0], nb[1]): KV blocks streamed for the tile
 };
 
-// Work tiles in order: with a causal mask the longest first (query block
-// descending), and within one query block the (b, h) pairs in order, so the
-// query heads sharing a K/V head run side by side.
+// Work tiles in launch order (the dynamic schedule hands them out in this
+// order, so it is also the order in which they start). A slice is one (b, head)
+// pair (b, K/V head with head packing); a slice has n_mblk query blocks and
+// n_splits key ranges. The slices are cut into groups of head_group
+// consecutive slices, about a fixed budget of K/V bytes each, and a group's
+// tiles run together so that its K/V stays in L2 while all of its query blocks
+// read it; within a group the query blocks run from the last (longest, with a
+// causal mask) to the first. With a causal mask the two shortest query-block
+// levels of every slice are left out of the groups and run at the very end,
+// longest first over all slices, so that the last tiles to start are short.
+// The query heads sharing a K/V head are adjacent slices, so they run side by side.
 // With head packing (pack_shift > 0, decode and short prefills) a tile belongs
 // to one K/V head: each 128-row sub-tile holds 128 >> pack_shift query rows of
 // all 2^pack_shift query heads of the group (row r of the sub-tile is query
@@ -161,13 +175,31 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const FwdParams& p) {
     const int ps = PACK ? p.pack_shift : 0;
     const int heads = PACK ? p.Hkv : p.Hq;
     const int sub_rows = kBlockM >> ps;
-    const int bh_count = p.B * heads;
-    const int per_mb = bh_count * p.n_splits;
-    const int mb_rank = tile / per_mb;
-    const int rem = tile - mb_rank * per_mb;
-    const int split = rem / bh_count;
-    const int bh = rem - split * bh_count;
-    const int mb = CAUSAL ? (p.n_mblk - 1 - mb_rank) : mb_rank;
+    const int slices = p.B * heads;
+    const int tail_levels = CAUSAL ? min(2, p.n_mblk) : 0;     // the two shortest levels run last
+    const int head_levels = p.n_mblk - tail_levels;            // levels run inside the groups
+    const int grouped = slices * head_levels * p.n_splits;      // tiles of the group phase
+    int mb, split, bh;
+    if (tile < grouped) {
+        const int per_slice = head_levels * p.n_splits;
+        const int g0 = tile / (p.head_group * per_slice) * p.head_group;   // first slice of the group
+        const int gs = min(p.head_group, slices - g0);                      // slices in the group
+        const int local = tile - g0 * per_slice;
+        const int per_level = gs * p.n_splits;
+        const int level = local / per_level;
+        const int rem = local - level * per_level;
+        split = rem / gs;
+        bh = g0 + (rem - split * gs);
+        mb = CAUSAL ? (p.n_mblk - 1 - level) : level;
+    } else {
+        const int local = tile - grouped;
+        const int per_level = slices * p.n_splits;
+        const int level = local / per_level;
+        const int rem = local - level * per_level;
+        split = rem / slices;
+        bh = rem - split * slices;
+        mb = CAUSAL ? (tail_levels - 1 - level) : (head_levels + level);
+    }
     TileInfo t;
     t.b = bh / heads;
     const int hh = bh - t.b * heads;
@@ -650,7 +682,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, const uint8_t* smem_
     };
 
     if (!leader) return;
-    if (p.debug_stall) alive = wait_phase(bar(C::bStall), 0, sc);   // nothing ever arrives
+    if (p.flags & kFlagDebugStall) alive = wait_phase(bar(C::bStall), 0, sc);   // nothing ever arrives
     // Sizes of tile-ring entry k (the issuer reads only the block counts).
     const uint8_t* ring = smem_ptr + C::kTileOff;
     auto fetch = [&](uint32_t k, int& nb0, int& nb1) -> bool {
@@ -937,7 +969,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, const uint8_t* s
                 w[i] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
             }
             if (row_ok) {
-                if (p.o_vec8) {
+                if (p.flags & kFlagOVec8) {
                     ptx::st_global_v8(orow + 32 * c, w);
                     ptx::st_global_v8(orow + 32 * c + 16, w + 8);
                 } else {
