@@ -14,6 +14,9 @@ inputs resident in device memory. Prints ONE JSON line on rank 0.
              timed region
   roofline   the kernel against the measured dense bf16 tensor peak
   cpu_baseline  the FP64 oracle on this host's cores, on a bounded sample
+  configs    the other causal D=128 prefills (GQA B8 S4096 and long-context GQA
+             B1 S16384 by default), each timed the same way: value, roofline,
+             median and min launch time, clocks
 
 `--rope` runs the same workload with the rotary position embedding: each step
 rotates the keys once (bandwidth-bound pass) and runs the attention kernel that
@@ -292,6 +295,56 @@ def config_json(cfg, rope=False):
                   "around each launch"}
 
 
+def time_config(A, cfg, steps, warmup, dev, stream, flush, clocks, world, peak, peak_src):
+    """Device time of `steps` launches of the fused attention on one more workload,
+    measured like the headline (inputs resident, L2 flushed before each launch,
+    CUDA events around each launch, max over ranks)."""
+    q, k, v, mask = I.make_inputs(cfg)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = None if mask is None else mask.to(dev)
+    del q, k, v, mask
+    o = torch.empty_like(qd)
+    lse = torch.empty((cfg.B, cfg.Hq, cfg.Sq), dtype=torch.float32, device=dev)
+
+    def launch():
+        A.attention(qd, kd, vd, causal=cfg.causal, mask=md, out=o, lse=lse, stream=stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize(dev)
+    if A.attn_last_status(stream.cuda_stream) != A.ATTN_OK:
+        raise RuntimeError(f"kernel reported a device timeout during warm-up ({cfg.name})")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    for i in range(steps):
+        flush.zero_()
+        starts[i].record(stream)
+        launch()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t1 = time.time()
+    if A.attn_last_status(stream.cuda_stream) != A.ATTN_OK:
+        raise RuntimeError(f"kernel reported a device timeout in the timed region ({cfg.name})")
+    ms = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
+    max_s = reduce_max(sum(ms) / 1e3, dev)
+    achieved = cfg.flops / (sum(ms) / 1e3 / steps) / 1e12
+    return {
+        "value": whole_job_tflops(cfg.flops, steps, world, max_s), "unit": UNIT, "steps": steps, "warmup": warmup,
+        "ms_per_step": max_s / steps * 1e3, "config": config_json(cfg),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": profiled_traffic("attn_fwd_" + cfg.name),
+                     "peak_source": f"{peak_src} bf16_tflops (burst, kernel timed alone)",
+                     "kernel": "attn_fwd_kernel", "median_ms": statistics.median(ms), "min_ms": min(ms)},
+        "clocks": clocks.summary(t0, t1),
+        "gpu_launches": steps,
+    }
+
+
 def run_ours(args, cfg):
     import torch.distributed as dist
     from transformer_attention_02_gb300 import attn as A
@@ -410,6 +463,19 @@ def run_ours(args, cfg):
     h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) + (0 if mh is None else mh.numel() * 4)
     d2h = oh.numel() * oh.element_size() + lh.numel() * 4
 
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # The other causal D=128 prefills, measured the same way on the same GPU.
+    extra = {}
+    names = [n for n in (args.extra_configs.split(",") if args.extra_configs else []) if n and n != cfg.name]
+    if names and not args.rope:
+        del qd, kd, vd, o, lse, md
+        torch.cuda.empty_cache()
+        for name in names:
+            extra[name] = time_config(A, I.CONFIGS[name], max(3, min(args.steps, 200)), args.warmup, dev, stream,
+                                      flush, clocks, world, peak, peak_src)
+            torch.cuda.empty_cache()
+
     if rank == 0:
         clocks.stop()
     if world > 1:
@@ -419,8 +485,6 @@ def run_ours(args, cfg):
 
     flops = cfg.flops
     value = whole_job_tflops(flops, args.steps, world, max_s)
-    peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     per_launch_s = sum(kernel_ms) / 1e3 / args.steps
     achieved = flops / per_launch_s / 1e12
     traffic = profiled_traffic("attn_fwd_" + cfg.name + ("_rope" if args.rope else ""))
@@ -439,11 +503,13 @@ def run_ours(args, cfg):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "api": "attention_rope + explicit copies" if args.rope else
                        "attention_host (attn_fwd_host: pipelined host-buffer call)"},
-        "gpu_launches": args.steps * (2 if args.rope else 1),
+        "gpu_launches": args.steps * (2 if args.rope else 1) + sum(e["gpu_launches"] for e in extra.values()),
         "clocks": clocks.summary(t_wall0, t_wall1),
         "wall_s_timed_region": t_wall1 - t_wall0,
         "kernel_source_hash": kernel_source_hash(),
     }
+    if extra:
+        line["configs"] = extra
     if args.rope:
         kv_bytes = 2 * cfg.B * cfg.Sk * cfg.Hkv * cfg.D * 2          # read K, write rotated K
         med = statistics.median(key_ms)
@@ -647,6 +713,9 @@ def main(argv=None):
     ap.add_argument("--config", default=I.BENCH_CONFIG, choices=sorted(I.CONFIGS))
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-configs", default="gqa_prefill,long_gqa_prefill",
+                    help="more workloads timed after the headline one, reported under 'configs' "
+                         "(comma-separated; empty for none)")
     ap.add_argument("--decode", action="store_true", help="decode over a KV cache (split-key path)")
     ap.add_argument("--decode-config", default="gqa_decode", choices=sorted(I.DECODE_CONFIGS))
     ap.add_argument("--block", action="store_true",

@@ -231,14 +231,14 @@ class Sim:
     def reads_pending(self, res_name: str) -> bool:
         return any(res_name in item[1] for item in self.mma_queue if item[0] == "mma")
 
-    def tma_issue(self, bar: str, nbytes: int, res_name: str, tag):
+    def tma_issue(self, bar: str, nbytes: int, res_name: str, tag, owner: str = ""):
         if self.reads_pending(res_name):
             raise ProtocolError(f"TMA into {res_name} while an unexecuted MMA still reads it")
         st = self.res.get(res_name)
         if isinstance(st, tuple) and st and st[0] == "loading":
             raise ProtocolError(f"TMA into {res_name} while another copy into it is in flight")
         self.res[res_name] = ("loading", tag)
-        self.inflight.append((bar, nbytes, res_name, tag))
+        self.inflight.append((bar, nbytes, res_name, tag, owner))
 
     def expect(self, res_name: str, want, what: str):
         got = self.res.get(res_name)
@@ -363,15 +363,14 @@ def _rotate(sim: Sim, buf: int, half: int):
 
 
 def role_qload(sim: Sim, tiles):
-    """Q producer (warp 10) and producer of the tile ring: entries are handed
-    out in order with one more entry always published ahead of the tile whose
-    Q this warp loads (next_entry / next_work of the kernel); in the rotary
-    variant it also rotates rows 0-63."""
+    """Q producer (warp 10) and producer of the tile ring: each entry is
+    published when this warp is about to load that tile's Q (next_work of the
+    kernel); in the rotary variant it also rotates rows 0-63."""
     p = sim.p
     uses = [0] * p.q_bufs
     nq = 0
     entries = ring_entries(tiles)
-    st = {"produced": 0, "pend": 2, "pend_t": None, "clc": 0, "drained": False}
+    st = {"produced": 0, "clc": 0, "drained": False}
 
     def produce():
         k = st["produced"]
@@ -387,6 +386,7 @@ def role_qload(sim: Sim, tiles):
             yield ("tma", "clc", 1, "clc_resp", ("CLC", st["clc"]))
             ok = yield ("wait", "clc", st["clc"])
             if not ok:
+                yield ("drain", "clc", st["clc"])       # the response must land before the CTA exits
                 return -1, None
 
             def read(n=st["clc"]):
@@ -403,20 +403,9 @@ def role_qload(sim: Sim, tiles):
         st["produced"] += 1
         return (1 if entries[k] is not None else 0), entries[k]
 
-    def next_entry():
-        if st["pend"] == 2:
-            r, t = yield from produce()
-        else:
-            r, t = st["pend"], st["pend_t"]
-        if r > 0:
-            st["pend"], st["pend_t"] = yield from produce()
-        else:
-            st["pend"] = 2
-        return r, t
-
     def next_work():
         while True:
-            r, t = yield from next_entry()
+            r, t = yield from produce()
             if not (r > 0 and t.n == 0):
                 return r, t
 
@@ -781,7 +770,7 @@ def run(p: Params, seed: int = 0, timeouts: bool = False, bias: float = 0.5, max
         else:
             kind, obj = rng.choice(cands)
         if kind == "tma":
-            bar, nbytes, res_name, tag = sim.inflight.pop(obj)
+            bar, nbytes, res_name, tag, _owner = sim.inflight.pop(obj)
             sim.res[res_name] = tag
             sim.bars[bar].complete_tx(nbytes)
             continue
@@ -809,7 +798,7 @@ def run(p: Params, seed: int = 0, timeouts: bool = False, bias: float = 0.5, max
             sim.bars[op[1]].expect_tx(op[2])
             sim.bars[op[1]].arrive()
         elif k == "tma":
-            sim.tma_issue(op[1], op[2], op[3], op[4])
+            sim.tma_issue(op[1], op[2], op[3], op[4], pr.name)
         elif k == "mma":
             sim.mma_queue.append(op)
         elif k == "commit":
@@ -819,6 +808,9 @@ def run(p: Params, seed: int = 0, timeouts: bool = False, bias: float = 0.5, max
         else:
             raise ProtocolError(f"unknown op {op}")
         _advance(pr, val)
+        if pr.done and any(f[4] == pr.name for f in sim.inflight):
+            # a warp may leave only once the copies it started have landed
+            raise ProtocolError(f"{pr.name} left with an asynchronous copy in flight")
 
     if not sim.abort:
         if sim.inflight or sim.mma_queue:

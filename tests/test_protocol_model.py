@@ -142,14 +142,16 @@ MUTATIONS = {
     "ring_producer_skips_wait": ("    if k >= p.tile_slots:\n", "    if False:\n"),
     # one arrival too few frees a tile-ring entry (a consumer not counted)
     "ring_consumer_undercount": ("        return 1 + 1 + 8 + (1 if self.rope else 0)", "        return 1 + 8 + (1 if self.rope else 0)"),
+    # the producer leaves without waiting for a launch-control response in flight
+    "clc_drain_skipped": ('                yield ("drain", "clc", st["clc"])       # the response must land before the CTA exits\n', ""),
     # the producer reads the launch-control response without waiting for it
     "clc_wait_skipped": ('            ok = yield ("wait", "clc", st["clc"])', '            ok = True'),
     # the K/V producer stops draining its copies on shutdown
     "drain_skipped": ('            yield ("drain", f"kv_full{s}", last // S)', "            pass"),
 }
 
-MUTATION_CASES = [CASES[0], CASES[1], CASES[2], CASES[5], CASES[7], CASES[10], CASES[12], CASES[15],
-                  M.Params(B=2, Hq=4, Hkv=2, Sq=1200, Sk=1200, grid=1, tile_slots=2)]
+MUTATION_CASES = [CASES[0], CASES[1], CASES[2], CASES[5], CASES[7], CASES[10], CASES[12], CASES[15], CASES[16],
+                  M.Params(B=2, Hq=4, Hkv=2, Sq=1200, Sk=1200, grid=1, tile_slots=1)]
 
 
 def _mutant(name):
@@ -178,11 +180,12 @@ def test_planted_protocol_bug_is_caught(name):
         for seed in SEEDS:
             if _caught(mod, p=q, seed=seed, bias=(seed % 4) / 4):
                 return
-    for p in MUTATION_CASES[:3]:                       # shutdown mistakes show on the abort path
+    for p in MUTATION_CASES:                           # shutdown mistakes show on the abort path
         q = mod.Params(**p.__dict__)
         total = M.run(p, seed=0).steps
         for seed in SEEDS:
             for frac in (0.1, 0.3, 0.5, 0.7, 0.9):
-                if _caught(mod, p=q, seed=seed, timeouts=True, abort_at=max(2, int(total * frac))):
+                if _caught(mod, p=q, seed=seed, timeouts=True, abort_at=max(2, int(total * frac)),
+                           bias=(seed % 4) / 4):
                     return
     pytest.fail(f"planted protocol bug {name!r} was not detected")

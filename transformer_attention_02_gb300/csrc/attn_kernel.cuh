@@ -453,10 +453,12 @@ __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr
 }
 
 // ------------------------------------------------------------- Q producer
-// Produces the tile ring and loads the Q sub-tiles of each work tile. Each
-// entry is published one entry ahead of the tile whose Q this warp loads, so
-// that the roles that peek at the next tile (K/V producer, MMA issuer) never
-// wait on this warp's own Q waits. The lower sub-tile alternates between two
+// Produces the tile ring and loads the Q sub-tiles of each work tile. An entry
+// is published (and, past the CTA's own tile, taken over from an unstarted
+// CTA) only when this warp is about to load that tile's Q, one tile before the
+// CTA starts it: the later a tile is assigned, the better the dynamic schedule
+// balances the SMs. Every other role needs entry k only when it reaches tile k,
+// after this warp has loaded Q for it. The lower sub-tile alternates between two
 // buffers, so it is fetched as soon as the tile before the current one has
 // finished with it; the upper sub-tile reuses one buffer and is fetched while
 // the previous tile's last products and epilogue run. In the rotary variant
@@ -488,7 +490,11 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
             ptx::mbar_arrive_expect_tx(bar(C::bClc), 16);
             ptx::clc_try_cancel(resp, bar(C::bClc));
         }
-        if (!warp_wait(bar(C::bClc), clc_uses & 1u, sc)) return -1;
+        if (!warp_wait(bar(C::bClc), clc_uses & 1u, sc)) {
+            // Aborting: the response must still land before the CTA may exit.
+            drain_phase(bar(C::bClc), clc_uses & 1u, sc);
+            return -1;
+        }
         ++clc_uses;
         uint32_t x = 0;
         const bool got = ptx::clc_query(resp, x);
@@ -521,25 +527,11 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
         ++produced;
         return found;
     };
-    TileInfo pend;
-    int pend_state = 2;                         // 2: nothing published ahead
-    // The next entry in order, keeping one more entry published ahead of it.
-    auto next_entry = [&](TileInfo& t) -> int {
-        int r;
-        if (pend_state == 2) {
-            r = produce(t);
-        } else {
-            t = pend;
-            r = pend_state;
-        }
-        pend_state = r > 0 ? produce(pend) : 2;
-        return r;
-    };
     // The next tile with at least one key block (1), the end (0) or an abort (-1).
     auto next_work = [&](TileInfo& t) -> int {
         int r;
         do {
-            r = next_entry(t);
+            r = produce(t);
         } while (r > 0 && t.n == 0);
         return r;
     };
