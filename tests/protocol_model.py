@@ -130,7 +130,7 @@ def schedule(p: Params):
             w += 1
     slices = p.B * heads
     head_group = max(1, min(slices, p.head_group or slices))
-    tail_levels = min(2, n_mblk) if p.causal else 0
+    tail_levels = min(3, n_mblk) if p.causal else 0
     head_levels = n_mblk - tail_levels
     grouped = slices * head_levels * n_splits
     for tile in order:

@@ -161,7 +161,7 @@ struct TileInfo {
 // consecutive slices, about a fixed budget of K/V bytes each, and a group's
 // tiles run together so that its K/V stays in L2 while all of its query blocks
 // read it; within a group the query blocks run from the last (longest, with a
-// causal mask) to the first. With a causal mask the two shortest query-block
+// causal mask) to the first. With a causal mask the three shortest query-block
 // levels of every slice are left out of the groups and run at the very end,
 // longest first over all slices, so that the last tiles to start are short.
 // The query heads sharing a K/V head are adjacent slices, so they run side by side.
@@ -176,7 +176,7 @@ __device__ __forceinline__ TileInfo tile_info(int tile, const FwdParams& p) {
     const int heads = PACK ? p.Hkv : p.Hq;
     const int sub_rows = kBlockM >> ps;
     const int slices = p.B * heads;
-    const int tail_levels = CAUSAL ? min(2, p.n_mblk) : 0;     // the two shortest levels run last
+    const int tail_levels = CAUSAL ? min(3, p.n_mblk) : 0;     // the three shortest levels run last
     const int head_levels = p.n_mblk - tail_levels;            // levels run inside the groups
     const int grouped = slices * head_levels * p.n_splits;      // tiles of the group phase
     int mb, split, bh;
