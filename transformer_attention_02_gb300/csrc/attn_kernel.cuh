@@ -806,53 +806,59 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, const uint8_t* s
             // Each warp waits on its own; the warpgroup agrees on whether to go
             // on at the one named barrier of the block (before the hand-off of
             // P), where a warp whose wait ran out votes to stop.
+            const int key0 = (ti.kb0 + j) * kBlockN;
+            // x: raw scores, or (additive mask) logits in log2 units
+            float x[kBlockN];
+            if (ADDITIVE) {
+                // The row's mask values for this block are fetched before the wait
+                // for S, so that their latency overlaps it instead of sitting on the
+                // softmax's path in every block; S is then read in 32-column pieces
+                // and combined in place (the mask and S fit in the register budget).
+                const bool whole = key0 + kBlockN <= p.Sk;
+                if (mrow != nullptr && whole && p.mask_vec4 == 2) {
+#pragma unroll
+                    for (int c = 0; c < kBlockN / 8; ++c) ptx::ld_global_nc_v8(mrow + key0 + 8 * c, x + 8 * c);
+                } else if (mrow != nullptr && whole && p.mask_vec4 == 1) {
+                    const float4* m4 = reinterpret_cast<const float4*>(mrow + key0);
+#pragma unroll
+                    for (int c = 0; c < kBlockN / 4; ++c) {
+                        const float4 mv = __ldg(m4 + c);
+                        x[4 * c + 0] = mv.x;
+                        x[4 * c + 1] = mv.y;
+                        x[4 * c + 2] = mv.z;
+                        x[4 * c + 3] = mv.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kBlockN; ++c)
+                        x[c] = (mrow != nullptr && key0 + c < p.Sk) ? __ldg(mrow + key0 + c) : 0.f;
+                }
+            }
             const bool landed = __all_sync(0xffffffffu, wait_phase(bar(C::bSFull + wg), s_phase, sc));
             s_phase ^= 1u;
             if (landed) {
                 ptx::tc_fence_after_sync();
-                uint32_t sr[kBlockN];
-#pragma unroll
-                for (int c = 0; c < kBlockN / 32; ++c) ptx::tmem_ld32(tS + 32 * c, sr + 32 * c);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int c = 0; c < kBlockN / 32; ++c) ptx::reg_fence32(sr + 32 * c);
-
-                const int key0 = (ti.kb0 + j) * kBlockN;
                 const int vis = kv_lim - key0;                    // columns >= vis are hidden
-                // x: raw scores, or (additive mask) logits in log2 units
-                float x[kBlockN];
-#pragma unroll
-                for (int c = 0; c < kBlockN; ++c) x[c] = __uint_as_float(sr[c]);
                 if (ADDITIVE) {
 #pragma unroll
-                    for (int c = 0; c < kBlockN; ++c) x[c] *= sl;
-                    if (mrow != nullptr) {
-                        if (p.mask_vec4 == 2 && key0 + kBlockN <= p.Sk) {
-                            // Each lane reads its own row: 32-byte loads halve the cache lines
-                            // touched per load instruction compared with 16-byte ones.
+                    for (int c = 0; c < kBlockN / 32; ++c) {
+                        uint32_t sr[32];
+                        ptx::tmem_ld32(tS + 32 * c, sr);
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence32(sr);
 #pragma unroll
-                            for (int c = 0; c < kBlockN / 8; ++c) {
-                                float mv[8];
-                                ptx::ld_global_nc_v8(mrow + key0 + 8 * c, mv);
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) x[8 * c + i] = fmaf(mv[i], kLog2e, x[8 * c + i]);
-                            }
-                        } else if (p.mask_vec4 && key0 + kBlockN <= p.Sk) {
-                            const float4* m4 = reinterpret_cast<const float4*>(mrow + key0);
-#pragma unroll
-                            for (int c = 0; c < kBlockN / 4; ++c) {
-                                const float4 mv = __ldg(m4 + c);
-                                x[4 * c + 0] = fmaf(mv.x, kLog2e, x[4 * c + 0]);
-                                x[4 * c + 1] = fmaf(mv.y, kLog2e, x[4 * c + 1]);
-                                x[4 * c + 2] = fmaf(mv.z, kLog2e, x[4 * c + 2]);
-                                x[4 * c + 3] = fmaf(mv.w, kLog2e, x[4 * c + 3]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < kBlockN; ++c)
-                                if (key0 + c < p.Sk) x[c] = fmaf(__ldg(mrow + key0 + c), kLog2e, x[c]);
-                        }
+                        for (int i = 0; i < 32; ++i)
+                            x[32 * c + i] = fmaf(x[32 * c + i], kLog2e, __uint_as_float(sr[i]) * sl);
                     }
+                } else {
+                    uint32_t sr[kBlockN];
+#pragma unroll
+                    for (int c = 0; c < kBlockN / 32; ++c) ptx::tmem_ld32(tS + 32 * c, sr + 32 * c);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < kBlockN / 32; ++c) ptx::reg_fence32(sr + 32 * c);
+#pragma unroll
+                    for (int c = 0; c < kBlockN; ++c) x[c] = __uint_as_float(sr[c]);
                 }
                 if (vis < kBlockN) {
 #pragma unroll
