@@ -443,15 +443,15 @@ def role_qload(sim: Sim, tiles):
             b0, b1 = nq & 1, 2 + nq % p.q1_bufs
             if not (yield from load(b1, ti, 1)):
                 break
+            if not lower_rotated and not (yield from rotate(b0, nq >> 1)):
+                break
+            if not (yield from rotate(b1, nq // p.q1_bufs)):
+                break
             rn, tn = yield from next_work()
             if rn < 0:
                 break
             more = rn > 0
             if more and not (yield from load((nq + 1) & 1, tn, 0)):
-                break
-            if not lower_rotated and not (yield from rotate(b0, nq >> 1)):
-                break
-            if not (yield from rotate(b1, nq // p.q1_bufs)):
                 break
             if more and not (yield from rotate((nq + 1) & 1, (nq + 1) >> 1)):
                 break

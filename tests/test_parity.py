@@ -83,6 +83,16 @@ def test_prefill_configs_sampled(name):
     check(o, lse, q, k, v, mask, cfg.mask_kind, slices=_slices_for(cfg), label=name)
 
 
+@pytest.mark.parametrize("name", ["llama2_7b_prefill_d64", "gqa_prefill_d64"])
+def test_d64_prefill_configs_sampled(name):
+    """Head dimension 64 at full size (P in TMEM columns of its own)."""
+    cfg = I.CONFIGS[name]
+    q, k, v, mask = I.make_inputs(cfg)
+    o, lse = run_gpu(q, k, v, mask, cfg.causal)
+    full_scan(o, lse)
+    check(o, lse, q, k, v, mask, cfg.mask_kind, slices=_slices_for(cfg)[:3], label=name)
+
+
 def test_long_context_config_sampled():
     cfg = I.CONFIGS["long_gqa_prefill"]
     q, k, v, mask = I.make_inputs(cfg)

@@ -563,23 +563,23 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
             ++nq;
         }
     } else {
-        // Loads are issued as early as in the plain variant (the upper sub-tile
-        // of tile T as soon as its buffer is free, the next tile's lower one
-        // right after it); rotations follow in load order: the upper sub-tile
-        // of T as soon as it lands, then the next tile's lower one, which
-        // therefore is ready a whole tile ahead.
+        // The upper sub-tile of tile T is loaded as soon as its buffer is free
+        // and rotated as soon as it lands; then the next tile is assigned and
+        // its lower sub-tile loaded and rotated, a whole tile ahead of its use.
         TileInfo ti, tn;
         bool have = next_work(ti) > 0 && load(0, ti.m0, ti);
         bool lower_rotated = false;
         while (have) {
             const int b0 = nq & 1, b1 = 2 + nq % C::kQ1Bufs;
             if (!load(b1, ti.m0 + kBlockM, ti)) break;
+            if (!lower_rotated && !rotate(b0, nq >> 1, ti.m0)) break;
+            if (!rotate(b1, nq / C::kQ1Bufs, ti.m0 + kBlockM)) break;
+            // The next tile is taken over only now: this tile's upper sub-tile,
+            // which the MMA issuer needs first, is not held up by that request.
             const int rn = next_work(tn);
             if (rn < 0) break;
             const bool more = rn > 0;
             if (more && !load((nq + 1) & 1, tn.m0, tn)) break;
-            if (!lower_rotated && !rotate(b0, nq >> 1, ti.m0)) break;
-            if (!rotate(b1, nq / C::kQ1Bufs, ti.m0 + kBlockM)) break;
             if (more && !rotate((nq + 1) & 1, (nq + 1) >> 1, tn.m0)) break;
             lower_rotated = true;
             ++nq;

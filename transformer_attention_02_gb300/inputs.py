@@ -85,6 +85,11 @@ for _d in (64, 128):
         _n = f"stress_d{_d}_{_v}"
         CONFIGS[_n] = _cfg(_n, 2, 16, 16, 2048, _d, False, additive_mask=True, values=_v)
 
+# The three causal prefills at head dimension 64 (the pages' other supported
+# size), for measurement.
+for _n in ("llama2_7b_prefill", "gqa_prefill", "long_gqa_prefill"):
+    CONFIGS[_n + "_d64"] = CONFIGS[_n].with_(name=_n + "_d64", D=64)
+
 BENCH_CONFIG = "llama2_7b_prefill"
 
 # Decode over a KV cache (one new query row per sequence; split-key path):
