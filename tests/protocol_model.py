@@ -79,12 +79,8 @@ class Params:
         return 4 if self.D == 128 else 8
 
     @property
-    def q1_bufs(self) -> int:
-        return 1
-
-    @property
     def q_bufs(self) -> int:
-        return 2 + self.q1_bufs
+        return 3
 
 
 @dataclass(frozen=True)
@@ -346,6 +342,19 @@ def role_tma(sim: Sim, tiles):
             yield ("drain", f"kv_full{s}", last // S)
 
 
+def q_slot(nq: int, t: int, nbufs: int = 3):
+    """Buffer and use count of sub-tile t of the nq-th tile with key blocks.
+    Sub-tiles take the Q buffers in turn (lower, upper, next lower, ...): with
+    three buffers the next tile's upper sub-tile goes into the buffer the
+    current lower sub-tile frees one block before the tile ends."""
+    i = 2 * nq + t
+    return i % nbufs, i // nbufs
+
+
+def q_bufs_of(nq: int, nbufs: int = 3):
+    return q_slot(nq, 0, nbufs)[0], q_slot(nq, 1, nbufs)[0]
+
+
 def _q_tag(ti: Tile, t: int, p: Params):
     return ("Q", ti.b, ti.h, ti.m0 + t * (BLOCK_M >> p.pack_shift))
 
@@ -419,8 +428,8 @@ def role_qload(sim: Sim, tiles):
         uses[buf] += 1
         return True
 
-    def rotate(buf, use):
-        ok = yield ("wait", f"q_full{buf}", use)
+    def rotate(buf):
+        ok = yield ("wait", f"q_full{buf}", uses[buf] - 1)     # its latest load
         if not ok:
             return False
         yield _rotate(sim, buf, 0)
@@ -432,28 +441,30 @@ def role_qload(sim: Sim, tiles):
             r, ti = yield from next_work()
             if r <= 0:
                 break
-            if not (yield from load(nq & 1, ti, 0)) or not (yield from load(2 + nq % p.q1_bufs, ti, 1)):
+            lb, ub = q_bufs_of(nq, p.q_bufs)
+            if not (yield from load(lb, ti, 0)) or not (yield from load(ub, ti, 1)):
                 break
             nq += 1
     else:
         r, ti = yield from next_work()
-        have = r > 0 and (yield from load(0, ti, 0))
+        have = r > 0 and (yield from load(q_bufs_of(0, p.q_bufs)[0], ti, 0))
         lower_rotated = False
         while have:
-            b0, b1 = nq & 1, 2 + nq % p.q1_bufs
+            b0, b1 = q_bufs_of(nq, p.q_bufs)
             if not (yield from load(b1, ti, 1)):
                 break
-            if not lower_rotated and not (yield from rotate(b0, nq >> 1)):
+            if not lower_rotated and not (yield from rotate(b0)):
                 break
-            if not (yield from rotate(b1, nq // p.q1_bufs)):
+            if not (yield from rotate(b1)):
                 break
             rn, tn = yield from next_work()
             if rn < 0:
                 break
             more = rn > 0
-            if more and not (yield from load((nq + 1) & 1, tn, 0)):
+            nb0 = q_bufs_of(nq + 1, p.q_bufs)[0]
+            if more and not (yield from load(nb0, tn, 0)):
                 break
-            if more and not (yield from rotate((nq + 1) & 1, (nq + 1) >> 1)):
+            if more and not (yield from rotate(nb0)):
                 break
             lower_rotated = True
             nq += 1
@@ -476,14 +487,13 @@ def role_rope_q(sim: Sim, tiles):
         k += 1
         if ti.n == 0:
             continue
-        bufs = (nq & 1, 2 + nq % p.q1_bufs)
-        uses = (nq >> 1, nq // p.q1_bufs)
         for t in range(2):
-            ok = yield ("wait", f"q_full{bufs[t]}", uses[t])
+            buf, use = q_slot(nq, t, p.q_bufs)
+            ok = yield ("wait", f"q_full{buf}", use)
             if not ok:
                 return
-            yield _rotate(sim, bufs[t], 1)
-            yield ("arrive", f"q_rdy{bufs[t]}")
+            yield _rotate(sim, buf, 1)
+            yield ("arrive", f"q_rdy{buf}")
         nq += 1
 
 
@@ -566,8 +576,8 @@ def role_mma(sim: Sim, tiles):
         n, n0, n1 = ti.n, ti.nb[0], ti.nb[1]
         if n == 0:                  # no key block: nothing to issue
             continue
-        q_buf = (nq & 1, 2 + nq % p.q1_bufs)
-        ok = yield ("wait", f"{q_ready}{q_buf[0]}", nq >> 1)
+        q_buf = q_bufs_of(nq, p.q_bufs)
+        ok = yield ("wait", f"{q_ready}{q_buf[0]}", q_slot(nq, 0, p.q_bufs)[1])
         if ok:
             ks, ok = yield from acquire()
         if not ok:
@@ -577,7 +587,7 @@ def role_mma(sim: Sim, tiles):
             yield _qk(sim, ti, 0, q_buf[0], ks, 0)
             yield ("commit", "s_full0")
         issued = True
-        ok = yield ("wait", f"{q_ready}{q_buf[1]}", nq // p.q1_bufs)
+        ok = yield ("wait", f"{q_ready}{q_buf[1]}", q_slot(nq, 1, p.q_bufs)[1])
         if not ok:
             alive = False
             break
@@ -586,8 +596,10 @@ def role_mma(sim: Sim, tiles):
             yield _qk(sim, ti, 1, q_buf[1], ks, 0)
             yield ("commit", "s_full1")
         yield ("commit", f"kv_empty{ks}")
-        if n == 1:
+        # each Q buffer is released after its sub-tile's last Q K^T
+        if n0 <= 1:
             yield ("commit", f"q_empty{q_buf[0]}")
+        if n1 <= 1:
             yield ("commit", f"q_empty{q_buf[1]}")
         v_seen = False
         for j in range(n):
@@ -612,6 +624,8 @@ def role_mma(sim: Sim, tiles):
                 if j + 1 < n0:
                     yield _qk(sim, ti, 0, q_buf[0], ks, j + 1)
                     yield ("commit", "s_full0")
+                    if j + 1 == n0 - 1:
+                        yield ("commit", f"q_empty{q_buf[0]}")
             if j < n1:
                 if not (yield from wait_p(1)):
                     alive = False
@@ -626,8 +640,7 @@ def role_mma(sim: Sim, tiles):
                     yield _qk(sim, ti, 1, q_buf[1], ks, j + 1)
                     yield ("commit", "s_full1")
                 yield ("commit", f"kv_empty{ks}")
-                if j + 1 == n - 1:
-                    yield ("commit", f"q_empty{q_buf[0]}")
+                if j + 1 == n1 - 1:
                     yield ("commit", f"q_empty{q_buf[1]}")
     if issued:
         yield ("commit", "drain")

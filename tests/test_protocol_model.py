@@ -90,7 +90,7 @@ MUTATIONS = {
     # V before K in the ring: the issuer takes the wrong tiles
     "ring_order_swapped": ('("KV", kv, ti.b, ti.hk, ti.kb0 + blk)', '("KV", 1 - kv, ti.b, ti.hk, ti.kb0 + blk)'),
     # Q buffers released one block early
-    "q_release_early": ("                if j + 1 == n - 1:\n", "                if j + 2 == n - 1 or (n == 2 and j == 0):\n"),
+    "q_release_early": ("                    if j + 1 == n0 - 1:\n", "                    if j + 2 == n0 - 1:\n"),
     # the next S_t written before P_t has been consumed
     "qk_before_pv": (
         "            if j < n0:\n"
@@ -136,8 +136,8 @@ MUTATIONS = {
     # the softmax counts its S phases per tile instead of continuously
     "softmax_phase_reset": ("        ok = True\n        for j in range(nb):", "        ok = True\n        s_cnt = 0\n        for j in range(nb):"),
     # the issuer waits for Q of the upper sub-tile on the lower sub-tile's buffer
-    "q_buffer_mixup": ('ok = yield ("wait", f"{q_ready}{q_buf[1]}", nq // p.q1_bufs)',
-                       'ok = yield ("wait", f"{q_ready}{q_buf[0]}", nq >> 1)'),
+    "q_buffer_mixup": ('ok = yield ("wait", f"{q_ready}{q_buf[1]}", q_slot(nq, 1, p.q_bufs)[1])',
+                       'ok = yield ("wait", f"{q_ready}{q_buf[0]}", q_slot(nq, 0, p.q_bufs)[1])'),
     # the tile-ring producer overwrites entries without waiting for them to be freed
     "ring_producer_skips_wait": ("    if k >= p.tile_slots:\n", "    if False:\n"),
     # one arrival too few frees a tile-ring entry (a consumer not counted)

@@ -106,10 +106,8 @@ struct TileCfg {
     static constexpr int kBoxBytes = 128 * kBoxCols * 2;      // 128 rows x 128 bytes
     static constexpr int kTileBytes = kBoxes * kBoxBytes;     // 128 rows x D
     static constexpr int kSlots = (D == 128) ? 4 : 8;         // K/V ring (K and V alternate)
-    // Q sub-tile buffers: the lower sub-tile alternates between buffers 0 and 1
-    // (so the next tile's is loaded a whole tile ahead), the upper uses buffer 2.
-    static constexpr int kQ1Bufs = 1;                         // buffers of the upper sub-tile
-    static constexpr int kQBufs = 2 + kQ1Bufs;
+    // Q sub-tile buffers, taken in turn by the sub-tiles (see q_slot).
+    static constexpr int kQBufs = 3;
     static constexpr int kQOff = 0;
     static constexpr int kKVOff = kQBufs * kTileBytes;
     static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
@@ -425,6 +423,18 @@ __device__ __forceinline__ void rope_rotate_rows(uint8_t* tile, int r_begin, int
     __syncwarp();
 }
 
+// Q buffer of sub-tile t (0 lower, 1 upper) of the nq-th tile with key blocks,
+// and which use of that buffer it is. Sub-tiles take the three buffers in turn
+// (lower, upper, next lower, ...): the next tile's lower sub-tile goes into the
+// buffer the previous tile's upper sub-tile has freed, a whole tile ahead, and
+// its upper sub-tile into the buffer the current lower sub-tile frees after its
+// last Q K^T, one key block before the current tile ends.
+__device__ __forceinline__ uint32_t q_slot(uint32_t nq, int t, uint32_t& use) {
+    const uint32_t i = 2u * nq + (uint32_t)t;
+    use = i / 3u;
+    return i - 3u * use;
+}
+
 // Rotary variant, warp 11: rotates rows 64..127 of every Q sub-tile once its
 // load has landed (the Q warp does rows 0..63), in the order the Q warp loads
 // them, and signals "Q ready" (two arrivals per use).
@@ -440,13 +450,13 @@ __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr
         TileInfo ti;
         if (!fetch_tile_warp(bar(C::bTileFull), bar(C::bTileEmpty), ring, k, ti, sc) || ti.n < 0) return;
         if (ti.n == 0) continue;
-        const int buf[2] = {(int)(nq & 1u), 2 + (int)(nq % C::kQ1Bufs)};
-        const uint32_t use[2] = {nq >> 1, nq / C::kQ1Bufs};
         for (int t = 0; t < 2; ++t) {
-            if (!warp_wait(bar(C::bQFull + buf[t]), use[t] & 1u, sc)) return;
-            rope_rotate_rows<D, BF16>(smem_ptr + C::kQOff + buf[t] * C::kTileBytes, kBlockM / 2, kBlockM,
+            uint32_t use;
+            const uint32_t buf = q_slot(nq, t, use);
+            if (!warp_wait(bar(C::bQFull + buf), use & 1u, sc)) return;
+            rope_rotate_rows<D, BF16>(smem_ptr + C::kQOff + buf * C::kTileBytes, kBlockM / 2, kBlockM,
                                       ti.m0 + t * kBlockM, p);
-            if (leader) ptx::mbar_arrive(bar(C::bQRdy + buf[t]));
+            if (leader) ptx::mbar_arrive(bar(C::bQRdy + buf));
         }
         ++nq;
     }
@@ -458,11 +468,11 @@ __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr
 // CTA) only when this warp is about to load that tile's Q, one tile before the
 // CTA starts it: the later a tile is assigned, the better the dynamic schedule
 // balances the SMs. Every other role needs entry k only when it reaches tile k,
-// after this warp has loaded Q for it. The lower sub-tile alternates between two
-// buffers, so it is fetched as soon as the tile before the current one has
-// finished with it; the upper sub-tile reuses one buffer and is fetched while
-// the previous tile's last products and epilogue run. In the rotary variant
-// this warp also rotates rows 0..63 of each sub-tile after it lands.
+// after this warp has loaded Q for it. The sub-tiles take the Q buffers in turn
+// (q_slot): the next tile's lower sub-tile is fetched as soon as the previous
+// tile's upper one is done, and its upper sub-tile while the current tile's
+// last key block runs. In the rotary variant this warp also rotates rows 0..63
+// of each sub-tile after it lands.
 template <int D, bool CAUSAL, bool BF16, bool ROPE, bool PACK>
 __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t smem, uint8_t* smem_ptr,
                            const SyncCtx& sc) {
@@ -549,8 +559,8 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
         ++uses[buf];
         return true;
     };
-    auto rotate = [&](int buf, uint32_t use, int row0) -> bool {
-        if (!warp_wait(bar(C::bQFull + buf), use & 1u, sc)) return false;
+    auto rotate = [&](int buf, int row0) -> bool {      // the buffer's latest load
+        if (!warp_wait(bar(C::bQFull + buf), (uses[buf] - 1) & 1u, sc)) return false;
         rope_rotate_rows<D, BF16>(smem_ptr + C::kQOff + buf * C::kTileBytes, 0, kBlockM / 2, row0, p);
         if (leader) ptx::mbar_arrive(bar(C::bQRdy + buf));
         return true;
@@ -558,8 +568,9 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
     if (!ROPE) {
         TileInfo ti;
         while (next_work(ti) > 0) {
-            if (!load(nq & 1, ti.m0, ti) || !load(2 + nq % C::kQ1Bufs, ti.m0 + (kBlockM >> (PACK ? p.pack_shift : 0)), ti))
-                break;
+            uint32_t use;
+            const int b0 = (int)q_slot(nq, 0, use), b1 = (int)q_slot(nq, 1, use);
+            if (!load(b0, ti.m0, ti) || !load(b1, ti.m0 + (kBlockM >> (PACK ? p.pack_shift : 0)), ti)) break;
             ++nq;
         }
     } else {
@@ -567,20 +578,22 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
         // and rotated as soon as it lands; then the next tile is assigned and
         // its lower sub-tile loaded and rotated, a whole tile ahead of its use.
         TileInfo ti, tn;
-        bool have = next_work(ti) > 0 && load(0, ti.m0, ti);
+        uint32_t use;
+        bool have = next_work(ti) > 0 && load((int)q_slot(0, 0, use), ti.m0, ti);
         bool lower_rotated = false;
         while (have) {
-            const int b0 = nq & 1, b1 = 2 + nq % C::kQ1Bufs;
+            const int b0 = (int)q_slot(nq, 0, use), b1 = (int)q_slot(nq, 1, use);
             if (!load(b1, ti.m0 + kBlockM, ti)) break;
-            if (!lower_rotated && !rotate(b0, nq >> 1, ti.m0)) break;
-            if (!rotate(b1, nq / C::kQ1Bufs, ti.m0 + kBlockM)) break;
+            if (!lower_rotated && !rotate(b0, ti.m0)) break;
+            if (!rotate(b1, ti.m0 + kBlockM)) break;
             // The next tile is taken over only now: this tile's upper sub-tile,
             // which the MMA issuer needs first, is not held up by that request.
             const int rn = next_work(tn);
             if (rn < 0) break;
             const bool more = rn > 0;
-            if (more && !load((nq + 1) & 1, tn.m0, tn)) break;
-            if (more && !rotate((nq + 1) & 1, (nq + 1) >> 1, tn.m0)) break;
+            const int nb0 = (int)q_slot(nq + 1, 0, use);
+            if (more && !load(nb0, tn.m0, tn)) break;
+            if (more && !rotate(nb0, tn.m0)) break;
             lower_rotated = true;
             ++nq;
             ti = tn;
@@ -620,7 +633,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, const uint8_t* smem_
     constexpr uint32_t kIdescPV = ptx::idesc_f16(128, D, BF16, false, true);
     // Base descriptors; a k-step advances the 16-byte-unit start address field.
     const uint64_t q_desc0 = ptx::sdesc_kmajor_sw128(smem + C::kQOff);
-    uint32_t q_buf[2] = {0, 2};                  // Q buffers of the current tile's sub-tiles
+    uint32_t q_buf[2] = {0, 1};                  // Q buffers of the current tile's sub-tiles
     const uint64_t kv_desc0 = ptx::sdesc_kmajor_sw128(smem + C::kKVOff);
     const uint64_t v_desc0 = ptx::sdesc_mnmajor_sw128(smem + C::kKVOff, C::kBoxBytes);
     uint32_t kv_use = 0, nq = 0;
@@ -691,25 +704,23 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, const uint8_t* smem_
         if (!fetch(k, n0, n1) || n1 < 0) break;      // n1 < 0: end marker
         const int n = max(n0, n1);      // n0, n1 are n or n - 1
         if (n == 0) continue;           // no key block for any row: nothing to issue
-        // Q buffers of this tile: lower sub-tile in buffer nq & 1 (its (nq >> 1)-th
-        // use), upper sub-tile in buffer 2 (its nq-th use). Both phases are consumed
-        // even when a sub-tile has no block, to keep the parities in step.
-        q_buf[0] = nq & 1u;
-        q_buf[1] = 2 + nq % C::kQ1Bufs;
-        auto release_q = [&]() {
-            commit(C::bQEmpty + q_buf[0]);
-            commit(C::bQEmpty + q_buf[1]);
-        };
+        // Q buffers of this tile (q_slot). Both are waited for even when a
+        // sub-tile has no block, to keep the parities in step; each is released
+        // after its sub-tile's last Q K^T.
+        uint32_t use0, use1;
+        q_buf[0] = q_slot(nq, 0, use0);
+        q_buf[1] = q_slot(nq, 1, use1);
         uint32_t ks, vs;
-        if (!wait_phase(bar(kQReady + q_buf[0]), (nq >> 1) & 1u, sc) || !acquire(ks)) { alive = false; break; }
+        if (!wait_phase(bar(kQReady + q_buf[0]), use0 & 1u, sc) || !acquire(ks)) { alive = false; break; }
         if (n0 > 0) issue_qk(0, q_buf[0], ks);
         issued = true;
-        if (!wait_phase(bar(kQReady + q_buf[1]), (nq / C::kQ1Bufs) & 1u, sc)) { alive = false; break; }
+        if (!wait_phase(bar(kQReady + q_buf[1]), use1 & 1u, sc)) { alive = false; break; }
         ptx::tc_fence_after_sync();
         ++nq;
         if (n1 > 0) issue_qk(1, q_buf[1], ks);
         commit(C::bKVEmpty + ks);
-        if (n == 1) release_q();
+        if (n0 <= 1) commit(C::bQEmpty + q_buf[0]);
+        if (n1 <= 1) commit(C::bQEmpty + q_buf[1]);
         bool v_seen = false;
         for (int j = 0; j < n; ++j) {
             const bool more = j + 1 < n;
@@ -722,7 +733,10 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, const uint8_t* smem_
             }
             if (more) {
                 if (!acquire(ks, k_seen)) { alive = false; break; }
-                if (j + 1 < n0) issue_qk(0, q_buf[0], ks);
+                if (j + 1 < n0) {
+                    issue_qk(0, q_buf[0], ks);
+                    if (j + 2 == n0) commit(C::bQEmpty + q_buf[0]);
+                }
             }
             if (j < n1) {
                 if (!wait_p(1)) { alive = false; break; }
@@ -734,7 +748,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, const uint8_t* smem_
                 v_seen = probe_next();
                 if (j + 1 < n1) issue_qk(1, q_buf[1], ks);
                 commit(C::bKVEmpty + ks);
-                if (j + 1 == n - 1) release_q();
+                if (j + 2 == n1) commit(C::bQEmpty + q_buf[1]);
             }
         }
     }
