@@ -80,8 +80,8 @@ constexpr int kTmaWarp = 9;
 constexpr int kQWarp = 10;
 constexpr int kRopeWarp = 11;               // second rotating warp of the rotary variant
 // Register split: launched at 168 per thread (384 x 168 = 64512), then the
-// softmax warpgroups grow to 200 and the MMA/TMA warpgroup shrinks to 104:
-// 128 x (200 + 200 + 104) = 64512. The host refuses to launch unless the
+// softmax warpgroups grow to 192 and the MMA/TMA warpgroup shrinks to 120:
+// 128 x (192 + 192 + 120) = 64512. The host refuses to launch unless the
 // compiled kernel uses exactly kLaunchRegs, so the split always fits.
 constexpr int kLaunchRegs = 168;
 constexpr uint32_t kSoftmaxRegs = 192;
