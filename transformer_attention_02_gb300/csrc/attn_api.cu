@@ -48,6 +48,7 @@ struct DeviceInfo {
     void* noalloc_scratch = nullptr;    // device address of the allocation-free scratch array
     bool smem_attr_set[2][4][2][3] = {};   // [D is 128][mask kind][bf16][plain, rotary, packed]
     bool gemm_attr_set = false;
+    bool ln_attr_set[3] = {};
 };
 
 std::mutex g_mutex;
@@ -756,9 +757,10 @@ int attn_layernorm(const void* x, const void* gamma, const void* beta, void* y, 
     DeviceInfo* dev = nullptr;
     int rc = device_info(&dev);
     if (rc != ATTN_OK) return rc;
-    return attn::launch_layernorm(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(gamma),
-                                  static_cast<const uint16_t*>(beta), static_cast<uint16_t*>(y), M, H,
-                                  layernorm_eps(eps), dev->num_sms, reinterpret_cast<cudaStream_t>(stream));
+    return attn::launch_layernorm(dev->ln_attr_set, static_cast<const uint16_t*>(x),
+                                  static_cast<const uint16_t*>(gamma), static_cast<const uint16_t*>(beta),
+                                  static_cast<uint16_t*>(y), M, H, layernorm_eps(eps), dev->num_sms,
+                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_fwd_qkvpacked(const void* qkv, void* o, float* lse, int B, int S, int Hq, int Hkv, int D, float scale,
@@ -801,9 +803,9 @@ int attn_block_fwd(const void* x, const void* ln_gamma, const void* ln_beta, con
     void* qkv = ws + L.qkv_off;
     void* a = ws + L.a_off;
     float* lse = reinterpret_cast<float*>(ws + L.lse_off);
-    rc = attn::launch_layernorm(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(ln_gamma),
-                                static_cast<const uint16_t*>(ln_beta), static_cast<uint16_t*>(n), M, hidden,
-                                layernorm_eps(eps), dev->num_sms, st);
+    rc = attn::launch_layernorm(dev->ln_attr_set, static_cast<const uint16_t*>(x),
+                                static_cast<const uint16_t*>(ln_gamma), static_cast<const uint16_t*>(ln_beta),
+                                static_cast<uint16_t*>(n), M, hidden, layernorm_eps(eps), dev->num_sms, st);
     if (rc != ATTN_OK) return rc;
     rc = linear_impl(*dev, n, w_qkv, b_qkv, nullptr, qkv, M, F, hidden, st);
     if (rc != ATTN_OK) return rc;

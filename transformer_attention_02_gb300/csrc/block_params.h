@@ -47,7 +47,9 @@ int launch(bool& attr_set, const CUtensorMap& a, const CUtensorMap& w, const Gem
 
 // LayerNorm of each of M rows of H bf16 values (H a multiple of 8, at most
 // 8192): y = (x - mean) / sqrt(var + eps) * gamma + beta, FP32 statistics.
-int launch_layernorm(const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, uint16_t* y, int M, int H,
-                     float eps, int num_sms, cudaStream_t stream);
+// attr_set caches, per context and kernel instance, that the kernel's
+// shared-memory attribute has been set.
+int launch_layernorm(bool (&attr_set)[3], const uint16_t* x, const uint16_t* gamma, const uint16_t* beta, uint16_t* y,
+                     int M, int H, float eps, int num_sms, cudaStream_t stream);
 
 }  // namespace attn
