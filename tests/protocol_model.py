@@ -59,6 +59,7 @@ class Params:
     Sk: int = 512
     num_splits: int = 1          # key ranges (split-key mode when > 1)
     rope: bool = False           # rotary variant: Q rotated by two warps, "Q ready" has two arrivals
+    additive: bool = False       # additive-mask variant: warpgroup 1's O leaves through its Q buffer
     pack_shift: int = 0          # GQA head packing: 2^pack_shift query heads share a tile's rows
     grid: int = 1                # persistent CTAs
     cta: int = 0                 # which CTA of the grid is modelled
@@ -81,6 +82,12 @@ class Params:
     @property
     def q_bufs(self) -> int:
         return 3
+
+    @property
+    def stage_o(self) -> bool:
+        """The upper sub-tile's O goes out through its Q buffer (additive-mask
+        variant at D = 128 with 16-bit output: no split keys, no head packing)."""
+        return self.additive and self.D == 128 and self.num_splits == 1 and self.pack_shift == 0
 
 
 @dataclass(frozen=True)
@@ -233,6 +240,8 @@ class Sim:
         st = self.res.get(res_name)
         if isinstance(st, tuple) and st and st[0] == "loading":
             raise ProtocolError(f"TMA into {res_name} while another copy into it is in flight")
+        if isinstance(st, tuple) and st and st[0] == "O":
+            raise ProtocolError(f"TMA into {res_name} over the staged O of {st[1]} not yet stored")
         self.res[res_name] = ("loading", tag)
         self.inflight.append((bar, nbytes, res_name, tag, owner))
 
@@ -379,7 +388,26 @@ def role_qload(sim: Sim, tiles):
     uses = [0] * p.q_bufs
     nq = 0
     entries = ring_entries(tiles)
-    st = {"produced": 0, "clc": 0, "drained": False}
+    st = {"produced": 0, "clc": 0, "drained": False, "staged": 0}
+    staged = [None] * p.q_bufs          # (staging index, tile key) of the O a buffer will hold
+
+    def store_staged(buf):
+        """Wait until warpgroup 1 has written the tile's O into buf, then copy it
+        out (the tensor store reads the buffer before this warp goes on). The
+        stagings alternate between two barriers: at most two are ever waiting
+        to be stored (the last two tiles' upper buffers), so no wait can fall
+        a whole phase behind."""
+        idx, key = staged[buf]
+        ok = yield ("wait", f"o_staged{idx % 2}", idx // 2)
+        if not ok:
+            return False
+
+        def store(buf=buf, key=key):
+            sim.expect(f"q{buf}", ("O", key), f"store of the staged O of {key}")
+            sim.res[f"q{buf}"] = "free"
+        yield ("act", store)
+        staged[buf] = None
+        return True
 
     def produce():
         k = st["produced"]
@@ -423,6 +451,11 @@ def role_qload(sim: Sim, tiles):
             ok = yield ("wait", f"q_empty{buf}", uses[buf] - 1)
             if not ok:
                 return False
+        if staged[buf] is not None and not (yield from store_staged(buf)):
+            return False
+        if p.stage_o and t == 1 and ti.nb[1] > 0:
+            staged[buf] = (st["staged"], _tile_key(ti))
+            st["staged"] += 1
         yield ("expect_tx", f"q_full{buf}", 1)
         yield ("tma", f"q_full{buf}", 1, f"q{buf}", _q_tag(ti, t, p))
         uses[buf] += 1
@@ -470,6 +503,10 @@ def role_qload(sim: Sim, tiles):
             nq += 1
             ti = tn
             have = more
+    # the O of the last tiles still waits in their buffers (in staging order)
+    for buf in sorted((b for b in range(p.q_bufs) if staged[b] is not None), key=lambda b: staged[b][0]):
+        if not (yield from store_staged(buf)):
+            break
     for b in range(p.q_bufs):
         if uses[b] > 0:
             yield ("drain", f"q_full{b}", uses[b] - 1)
@@ -648,10 +685,15 @@ def role_mma(sim: Sim, tiles):
 
 
 def role_softmax(sim: Sim, tiles, t: int):
-    """Softmax warpgroup t: per block, S_t -> P_t (rescaling O_t), then the epilogue."""
+    """Softmax warpgroup t: per block, S_t -> P_t (rescaling O_t), then the
+    epilogue; warpgroup 1 writes its O into the upper sub-tile's Q buffer
+    (stage_o) and signals the Q warp, which stores it."""
+    p = sim.p
     s_cnt = 0
     o_cnt = 0
     k = 0
+    nq = 0
+    n_staged = 0
     while True:
         ok, ti = yield from ring_fetch(sim, k, arrivals=4)     # each of the four warps frees the entry
         if not ok or ti is None:
@@ -659,6 +701,9 @@ def role_softmax(sim: Sim, tiles, t: int):
         k += 1
         nb = ti.nb[t]
         key = _tile_key(ti)
+        ubuf = q_slot(nq, 1, p.q_bufs)[0]
+        if ti.n > 0:
+            nq += 1
         if nb == 0:
             continue
         ok = True
@@ -687,6 +732,20 @@ def role_softmax(sim: Sim, tiles, t: int):
             sim.expect(f"O{t}", ("O", key, t, nb - 1), f"epilogue {t}")
             sim.res[f"O{t}"] = ("read", key, t)
         yield ("act", epi)
+        if p.stage_o and t == 1:
+            sidx = n_staged
+            n_staged += 1
+
+            def stage(ti=ti, ubuf=ubuf):
+                q = sim.res.get(f"q{ubuf}")
+                if not (isinstance(q, tuple) and q[:4] == _q_tag(ti, 1, p)[:4]):
+                    raise ProtocolError(f"staging the O of {key} into q{ubuf}, which holds {q}")
+                if sim.reads_pending(f"q{ubuf}"):
+                    raise ProtocolError(f"staging the O of {key} into q{ubuf} while an MMA still reads it")
+                sim.res[f"q{ubuf}"] = ("O", key)
+            yield ("act", stage)
+            for _ in range(4):                   # one arrival per warp, after its rows are written
+                yield ("arrive", f"o_staged{sidx % 2}")
 
 
 # ---------------------------------------------------------------- scheduler
@@ -702,6 +761,8 @@ def make_sim(p: Params, seed: int, timeouts: bool = False):
         sim.bars[f"tile_full{i}"] = Barrier(f"tile_full{i}", 1)
         sim.bars[f"tile_empty{i}"] = Barrier(f"tile_empty{i}", p.tile_consumers)
     sim.bars["clc"] = Barrier("clc", 1)
+    for i in range(2):
+        sim.bars[f"o_staged{i}"] = Barrier(f"o_staged{i}", 4)
     sim.bars["drain"] = Barrier("drain", 1)
     sim.bars["stall"] = Barrier("stall", 1)
     tiles = schedule(p)
@@ -832,6 +893,10 @@ def run(p: Params, seed: int = 0, timeouts: bool = False, bias: float = 0.5, max
             o = sim.res.get(f"O{t}", "free")
             if not (o == "free" or o[0] == "read"):
                 raise ProtocolError(f"O{t} not read out at the end: {o}")
+        for b in range(p.q_bufs):
+            q = sim.res.get(f"q{b}")
+            if isinstance(q, tuple) and q and q[0] == "O":
+                raise ProtocolError(f"the staged O of {q[1]} in q{b} was never stored")
     else:
         if sim.inflight or sim.mma_queue:
             raise ProtocolError("abort path ended with copies or MMAs in flight")

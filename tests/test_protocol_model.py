@@ -7,7 +7,8 @@ with the asynchronous TMA copies and the tensor core's in-order MMA queue. The
 cases cover both head dimensions (ring of 4 and 8 slots), causal and
 non-causal tiles with ragged tails and Sq != Sk, sub-tiles with no key block,
 GQA head packing, split-key mode, the rotary variant's two-arrival "Q ready"
-barriers, and the abort path (a stalled wait that runs out; an abort raised at
+barriers, the additive-mask variant's output staged in a Q buffer and stored
+by the Q warp, and the abort path (a stalled wait that runs out; an abort raised at
 an arbitrary moment). Planted protocol mistakes must each be caught.
 """
 import os
@@ -41,6 +42,12 @@ CASES = [
     M.Params(B=2, Hq=4, Hkv=2, Sq=1000, Sk=300, cta=0, steal_seed=2, D=64),
     M.Params(rope=True, B=2, Hq=2, Hkv=1, Sq=900, Sk=900, cta=1, steal_seed=3),
     M.Params(num_splits=3, Hq=4, Hkv=1, pack_shift=2, Sq=16, Sk=1500, cta=0, steal_seed=4),
+    # additive-mask variant: warpgroup 1's O staged in its Q buffer, stored by the Q warp
+    M.Params(additive=True),
+    M.Params(additive=True, causal=False, Sq=300, Sk=700),
+    M.Params(additive=True, B=2, Hq=4, Hkv=2, Sq=1200, Sk=1200, cta=3, steal_seed=1),
+    M.Params(additive=True, Sq=1000, Sk=300, B=2, Hq=2, Hkv=2, grid=2, cta=1),
+    M.Params(additive=True, num_splits=3, Sq=100, Sk=1500, grid=2, cta=1),     # split keys: no staging
 ]
 
 SEEDS = range(12)
@@ -48,7 +55,7 @@ SEEDS = range(12)
 
 def _id(p):
     return f"D{p.D}_c{int(p.causal)}_B{p.B}H{p.Hq}-{p.Hkv}_S{p.Sq}-{p.Sk}_sp{p.num_splits}_r{int(p.rope)}" \
-           f"_pk{p.pack_shift}_g{p.grid}.{p.cta}_st{p.steal_seed}"
+           f"_pk{p.pack_shift}_g{p.grid}.{p.cta}_st{p.steal_seed}_m{int(p.additive)}"
 
 
 @pytest.mark.parametrize("p", CASES, ids=_id)
@@ -58,7 +65,7 @@ def test_protocol_has_no_deadlock_or_race(p):
         M.run(p, seed=seed, bias=(seed % 4) / 4)
 
 
-@pytest.mark.parametrize("p", [CASES[0], CASES[1], CASES[7], CASES[10], CASES[15]], ids=_id)
+@pytest.mark.parametrize("p", [CASES[0], CASES[1], CASES[7], CASES[10], CASES[15], CASES[21]], ids=_id)
 def test_stalled_wait_aborts_every_role(p):
     """The stall hook: the MMA issuer waits on a barrier nothing signals; its
     wait runs out, and every role must then finish, shutdown waits included."""
@@ -68,7 +75,7 @@ def test_stalled_wait_aborts_every_role(p):
         assert sim.timed_out
 
 
-@pytest.mark.parametrize("p", [CASES[0], CASES[2], CASES[5], CASES[11], CASES[16]], ids=_id)
+@pytest.mark.parametrize("p", [CASES[0], CASES[2], CASES[5], CASES[11], CASES[16], CASES[19], CASES[22]], ids=_id)
 def test_abort_at_any_moment_terminates(p):
     """Some wait runs out at an arbitrary step: no role may hang afterwards."""
     total = M.run(p, seed=0).steps
@@ -146,11 +153,23 @@ MUTATIONS = {
     "clc_drain_skipped": ('                yield ("drain", "clc", st["clc"])       # the response must land before the CTA exits\n', ""),
     # the producer reads the launch-control response without waiting for it
     "clc_wait_skipped": ('            ok = yield ("wait", "clc", st["clc"])', '            ok = True'),
+    # the Q warp stores a staged O without waiting for warpgroup 1 to write it
+    "stage_wait_skipped": ('ok = yield ("wait", f"o_staged{idx % 2}", idx // 2)', 'ok = True'),
+    # the Q warp reloads a buffer that still holds a staged O
+    "stage_store_skipped": ("        if staged[buf] is not None and not (yield from store_staged(buf)):\n",
+                            "        if False:\n"),
+    # one warp of warpgroup 1 does not report its staged rows
+    "stage_arrival_missing": ('            for _ in range(4):                   # one arrival per warp, after its rows are written',
+                              '            for _ in range(3):'),
+    # the Q warp leaves without storing the last tiles' staged O
+    "stage_final_store_skipped": ("        if not (yield from store_staged(buf)):\n            break\n    for b in range(p.q_bufs):",
+                                  "        break\n    for b in range(p.q_bufs):"),
     # the K/V producer stops draining its copies on shutdown
     "drain_skipped": ('            yield ("drain", f"kv_full{s}", last // S)', "            pass"),
 }
 
 MUTATION_CASES = [CASES[0], CASES[1], CASES[2], CASES[5], CASES[7], CASES[10], CASES[12], CASES[15], CASES[16],
+                  CASES[19], CASES[21],
                   M.Params(B=2, Hq=4, Hkv=2, Sq=1200, Sk=1200, grid=1, tile_slots=1)]
 
 

@@ -210,24 +210,25 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
 
 template <int D, bool BF16, bool ROPE, bool PACK>
 int launch_d(DeviceInfo& dev, int mask_kind, const CUtensorMap& tq, const CUtensorMap& tk,
-             const CUtensorMap& tv, const attn::FwdParams& p, int grid, cudaStream_t stream) {
+             const CUtensorMap& tv, const CUtensorMap& to, const attn::FwdParams& p, int grid, cudaStream_t stream) {
     bool* attr = dev.smem_attr_set[D == 128][mask_kind][BF16 ? 1 : 0] + (ROPE ? 1 : PACK ? 2 : 0);
     switch (mask_kind) {
         case ATTN_MASK_NONE:
-            return attn::launch_fwd<D, false, false, BF16, ROPE, PACK>(*attr, tq, tk, tv, p, grid, stream);
+            return attn::launch_fwd<D, false, false, BF16, ROPE, PACK>(*attr, tq, tk, tv, to, p, grid, stream);
         case ATTN_MASK_CAUSAL:
-            return attn::launch_fwd<D, true, false, BF16, ROPE, PACK>(*attr, tq, tk, tv, p, grid, stream);
+            return attn::launch_fwd<D, true, false, BF16, ROPE, PACK>(*attr, tq, tk, tv, to, p, grid, stream);
         case ATTN_MASK_ADDITIVE:
-            return attn::launch_fwd<D, false, true, BF16, ROPE, PACK>(*attr, tq, tk, tv, p, grid, stream);
-        default: return attn::launch_fwd<D, true, true, BF16, ROPE, PACK>(*attr, tq, tk, tv, p, grid, stream);
+            return attn::launch_fwd<D, false, true, BF16, ROPE, PACK>(*attr, tq, tk, tv, to, p, grid, stream);
+        default: return attn::launch_fwd<D, true, true, BF16, ROPE, PACK>(*attr, tq, tk, tv, to, p, grid, stream);
     }
 }
 
 template <bool BF16, bool ROPE, bool PACK>
 int launch_any(DeviceInfo& dev, int D, int mask_kind, const CUtensorMap& tq, const CUtensorMap& tk,
-               const CUtensorMap& tv, const attn::FwdParams& p, int grid, cudaStream_t stream) {
-    return D == 128 ? launch_d<128, BF16, ROPE, PACK>(dev, mask_kind, tq, tk, tv, p, grid, stream)
-                    : launch_d<64, BF16, ROPE, PACK>(dev, mask_kind, tq, tk, tv, p, grid, stream);
+               const CUtensorMap& tv, const CUtensorMap& to, const attn::FwdParams& p, int grid,
+               cudaStream_t stream) {
+    return D == 128 ? launch_d<128, BF16, ROPE, PACK>(dev, mask_kind, tq, tk, tv, to, p, grid, stream)
+                    : launch_d<64, BF16, ROPE, PACK>(dev, mask_kind, tq, tk, tv, to, p, grid, stream);
 }
 
 // ------------------------------------------------ rotary position embedding
@@ -467,10 +468,11 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
         k = rope->k_rot;
     }
 
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (encode_bshd(&tq, q, B, Sq, Hq, D, bf16, q_stride, 1 << pack_shift) != ATTN_OK ||
         encode_bshd(&tk, k, B, Sk, Hkv, D, bf16, kv_stride) != ATTN_OK ||
-        encode_bshd(&tv, v, B, Sk, Hkv, D, bf16, kv_stride) != ATTN_OK)
+        encode_bshd(&tv, v, B, Sk, Hkv, D, bf16, kv_stride) != ATTN_OK ||
+        encode_bshd(&to, o, B, Sq, Hq, D, bf16) != ATTN_OK)       // O is always (B, Sq, Hq, D), contiguous
         return ATTN_ERR_CUDA;
 
     attn::FwdParams p{};
@@ -515,14 +517,14 @@ int attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* l
     // longest-first schedule.
     const int grid = p.n_tiles;
     if (rope)
-        rc = bf16 ? launch_any<true, true, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
-                  : launch_any<false, true, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);
+        rc = bf16 ? launch_any<true, true, false>(*dev, D, mask_kind, tq, tk, tv, to, p, grid, stream)
+                  : launch_any<false, true, false>(*dev, D, mask_kind, tq, tk, tv, to, p, grid, stream);
     else if (pack_shift)
-        rc = bf16 ? launch_any<true, false, true>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
-                  : launch_any<false, false, true>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);
+        rc = bf16 ? launch_any<true, false, true>(*dev, D, mask_kind, tq, tk, tv, to, p, grid, stream)
+                  : launch_any<false, false, true>(*dev, D, mask_kind, tq, tk, tv, to, p, grid, stream);
     else
-        rc = bf16 ? launch_any<true, false, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream)
-                  : launch_any<false, false, false>(*dev, D, mask_kind, tq, tk, tv, p, grid, stream);
+        rc = bf16 ? launch_any<true, false, false>(*dev, D, mask_kind, tq, tk, tv, to, p, grid, stream)
+                  : launch_any<false, false, false>(*dev, D, mask_kind, tq, tk, tv, to, p, grid, stream);
     if (rc != ATTN_OK || splits == 1) return rc;
 
     // ---- merge the key ranges

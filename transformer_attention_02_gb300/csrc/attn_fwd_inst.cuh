@@ -11,7 +11,7 @@ namespace attn {
 
 template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE, bool PACK>
 int launch_fwd(bool& attr_set, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const FwdParams& p, int grid, cudaStream_t stream) {
+               const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream) {
     auto kernel = attn_fwd_kernel<D, CAUSAL, ADDITIVE, BF16, ROPE, PACK>;
     constexpr int smem = TileCfg<D>::kSmemBytes;
     if (!attr_set) {
@@ -23,16 +23,16 @@ int launch_fwd(bool& attr_set, const CUtensorMap& tq, const CUtensorMap& tk, con
             return ATTN_ERR_CUDA;
         attr_set = true;
     }
-    kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+    kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace attn
 
 #define ATTN_INSTANTIATE_ONE(D, CAUSAL, ADDITIVE, BF16, ROPE, PACK)                                              \
-    template int attn::launch_fwd<D, CAUSAL, ADDITIVE, BF16, ROPE, PACK>(bool&, const CUtensorMap&,              \
-                                                                         const CUtensorMap&, const CUtensorMap&, \
-                                                                         const attn::FwdParams&, int, cudaStream_t);
+    template int attn::launch_fwd<D, CAUSAL, ADDITIVE, BF16, ROPE, PACK>(                                        \
+        bool&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,                      \
+        const attn::FwdParams&, int, cudaStream_t);
 
 #define ATTN_INSTANTIATE_FWD(BF16, ROPE, PACK)                  \
     ATTN_INSTANTIATE_ONE(64, false, false, BF16, ROPE, PACK)    \

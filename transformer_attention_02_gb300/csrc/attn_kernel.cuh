@@ -125,7 +125,8 @@ struct TileCfg {
     static constexpr int bTileFull = bQRdy + kQBufs;  // [kTileSlots] tile ring entry published
     static constexpr int bTileEmpty = bTileFull + kTileSlots;   // [kTileSlots] entry freed by every consumer
     static constexpr int bClc = bTileEmpty + kTileSlots;      // cluster-launch-control response landed
-    static constexpr int kNumBars = bClc + 1;
+    static constexpr int bOStaged = bClc + 1;         // [2] upper sub-tile's O staged (one arrival per warp)
+    static constexpr int kNumBars = bOStaged + 2;
     // tile ring: kTileSlots entries of 32 bytes, read and written as 16-byte vectors
     static constexpr int kTileOff = (kBarOff + 8 * kNumBars + 31) / 32 * 32;
     static constexpr int kClcOff = kTileOff + kTileSlots * 32;   // 16-byte cluster-launch-control response
@@ -423,6 +424,12 @@ __device__ __forceinline__ void rope_rotate_rows(uint8_t* tile, int r_begin, int
     __syncwarp();
 }
 
+// Variants whose upper sub-tile's O leaves through its Q buffer (role_softmax).
+template <int D, bool ADDITIVE, bool PACK>
+__host__ __device__ constexpr bool kStagesO() {
+    return ADDITIVE && !PACK && D == 128;
+}
+
 // Q buffer of sub-tile t (0 lower, 1 upper) of the nq-th tile with key blocks,
 // and which use of that buffer it is. Sub-tiles take the three buffers in turn
 // (lower, upper, next lower, ...): the next tile's lower sub-tile goes into the
@@ -473,9 +480,9 @@ __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr
 // tile's upper one is done, and its upper sub-tile while the current tile's
 // last key block runs. In the rotary variant this warp also rotates rows 0..63
 // of each sub-tile after it lands.
-template <int D, bool CAUSAL, bool BF16, bool ROPE, bool PACK>
-__device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t smem, uint8_t* smem_ptr,
-                           const SyncCtx& sc) {
+template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE, bool PACK>
+__device__ void role_qload(const CUtensorMap* tmQ, const CUtensorMap* tmO, const FwdParams& p, uint32_t smem,
+                           uint8_t* smem_ptr, const SyncCtx& sc) {
     using C = TileCfg<D>;
     const bool leader = (threadIdx.x & 31) == 0;
     const uint32_t bars = smem + C::kBarOff;
@@ -548,8 +555,42 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
 
     uint32_t uses[C::kQBufs] = {};              // loads issued into each buffer
     uint32_t nq = 0;                            // work tiles with at least one block
-    auto load = [&](int buf, int row0, const TileInfo& ti) -> bool {
+    // Staged output (see role_softmax): a buffer that held an upper sub-tile
+    // with blocks receives that tile's O from warpgroup 1; before the buffer
+    // is loaded again this warp waits for it (bOStaged, alternating between
+    // two barriers: at most the last two tiles' stagings are ever pending) and
+    // stores it by TMA. The store has read the buffer when wait_group.read
+    // returns, so the next load may then overwrite it.
+    constexpr bool kStaging = kStagesO<D, ADDITIVE, PACK>();
+    const bool stage_o = kStaging && p.o_part == nullptr;
+    constexpr int kSt = kStaging ? C::kQBufs : 1;
+    int st_idx[kSt], st_b[kSt], st_h[kSt], st_m[kSt];
+#pragma unroll
+    for (int b = 0; b < kSt; ++b) st_idx[b] = st_b[b] = st_h[b] = st_m[b] = -1;
+    int n_staged = 0;
+    auto store_staged = [&](int buf) -> bool {
+        const int idx = st_idx[buf];
+        if (!warp_wait(bar(C::bOStaged + (idx & 1)), ((uint32_t)idx >> 1) & 1u, sc)) return false;
+        if (leader) {
+            for (int c = 0; c < C::kBoxes; ++c)
+                ptx::tma_store_4d(tmO, smem + C::kQOff + buf * C::kTileBytes + c * C::kBoxBytes, c * C::kBoxCols,
+                                  st_h[buf], st_m[buf], st_b[buf]);
+            ptx::bulk_commit_group();
+            ptx::bulk_wait_group_read<0>();
+        }
+        __syncwarp();
+        st_idx[buf] = -1;
+        return true;
+    };
+    auto load = [&](int buf, int row0, const TileInfo& ti, bool upper) -> bool {
         if (uses[buf] > 0 && !warp_wait(bar(C::bQEmpty + buf), (uses[buf] - 1) & 1u, sc)) return false;
+        if (kStaging && st_idx[buf] >= 0 && !store_staged(buf)) return false;
+        if (kStaging && stage_o && upper && ti.nb[1] > 0) {
+            st_idx[buf] = n_staged++;
+            st_b[buf] = ti.b;
+            st_h[buf] = ti.h;
+            st_m[buf] = row0;
+        }
         if (leader) {
             ptx::mbar_arrive_expect_tx(bar(C::bQFull + buf), C::kTileBytes);
             for (int c = 0; c < C::kBoxes; ++c)
@@ -570,7 +611,8 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
         while (next_work(ti) > 0) {
             uint32_t use;
             const int b0 = (int)q_slot(nq, 0, use), b1 = (int)q_slot(nq, 1, use);
-            if (!load(b0, ti.m0, ti) || !load(b1, ti.m0 + (kBlockM >> (PACK ? p.pack_shift : 0)), ti)) break;
+            if (!load(b0, ti.m0, ti, false) || !load(b1, ti.m0 + (kBlockM >> (PACK ? p.pack_shift : 0)), ti, true))
+                break;
             ++nq;
         }
     } else {
@@ -579,11 +621,11 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
         // its lower sub-tile loaded and rotated, a whole tile ahead of its use.
         TileInfo ti, tn;
         uint32_t use;
-        bool have = next_work(ti) > 0 && load((int)q_slot(0, 0, use), ti.m0, ti);
+        bool have = next_work(ti) > 0 && load((int)q_slot(0, 0, use), ti.m0, ti, false);
         bool lower_rotated = false;
         while (have) {
             const int b0 = (int)q_slot(nq, 0, use), b1 = (int)q_slot(nq, 1, use);
-            if (!load(b1, ti.m0 + kBlockM, ti)) break;
+            if (!load(b1, ti.m0 + kBlockM, ti, true)) break;
             if (!lower_rotated && !rotate(b0, ti.m0)) break;
             if (!rotate(b1, ti.m0 + kBlockM)) break;
             // The next tile is taken over only now: this tile's upper sub-tile,
@@ -592,13 +634,25 @@ __device__ void role_qload(const CUtensorMap* tmQ, const FwdParams& p, uint32_t 
             if (rn < 0) break;
             const bool more = rn > 0;
             const int nb0 = (int)q_slot(nq + 1, 0, use);
-            if (more && !load(nb0, tn.m0, tn)) break;
+            if (more && !load(nb0, tn.m0, tn, false)) break;
             if (more && !rotate(nb0, tn.m0)) break;
             lower_rotated = true;
             ++nq;
             ti = tn;
             have = more;
         }
+    }
+    if constexpr (kStaging) {
+        // The last tiles' staged O (at most two buffers), in staging order.
+        for (int pass = 0; pass < 2; ++pass) {
+            int next = -1;
+#pragma unroll
+            for (int b = 0; b < C::kQBufs; ++b)
+                if (st_idx[b] >= 0 && (next < 0 || st_idx[b] < st_idx[next])) next = b;
+            if (next < 0 || !store_staged(next)) break;
+        }
+        if (leader) ptx::bulk_wait_group<0>();    // every store issued here has completed
+        __syncwarp();
     }
     // Shut down: wait until every copy this warp started has landed.
     for (int b = 0; b < C::kQBufs; ++b)
@@ -761,7 +815,7 @@ __device__ void role_mma(const FwdParams& p, uint32_t smem, const uint8_t* smem_
 
 // ------------------------------------------------ softmax / epilogue warpgroup
 template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool PACK>
-__device__ void role_softmax(const FwdParams& p, uint32_t smem, const uint8_t* smem_ptr, uint32_t tmem, int wg,
+__device__ void role_softmax(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr, uint32_t tmem, int wg,
                              const SyncCtx& sc) {
     using C = TileCfg<D>;
     const uint32_t bars = smem + C::kBarOff;
@@ -774,12 +828,24 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, const uint8_t* s
     constexpr float kLn2 = 0.6931471805599453f;
     constexpr float kLog2e = 1.4426950408889634f;
     uint32_t s_phase = 0, o_phase = 0;
+    // With an additive mask and D = 128, warpgroup 1 (16-bit output, no split
+    // keys, no head packing) writes its O into the upper sub-tile's Q buffer,
+    // free once "O ready" has arrived, and the Q warp stores it by TMA
+    // (role_qload): its epilogue then skips the row-strided global stores,
+    // which compete with the mask rows' loads for the L1 (those loads bound
+    // the masked kernel). Without a mask, or at D = 64, the direct stores are
+    // as fast or faster.
+    const bool stage = kStagesO<D, ADDITIVE, PACK>() && wg == 1 && p.o_part == nullptr;
+    uint32_t nq = 0, n_staged = 0;                            // tiles with blocks; O staged so far
 
     const uint8_t* ring = smem_ptr + C::kTileOff;
     for (uint32_t k = 0;; ++k) {
         TileInfo ti;
         if (!fetch_tile_warp(bar(C::bTileFull), bar(C::bTileEmpty), ring, k, ti, sc)) return;
         if (ti.n < 0) break;                                  // end marker
+        uint32_t use_unused;
+        const uint32_t ubuf = q_slot(nq, 1, use_unused);      // this tile's upper Q buffer
+        if (ti.n > 0) ++nq;
         const int nb = ti.nb[wg];
         const int ps = PACK ? p.pack_shift : 0;
         const int row = ti.m0 + ((wg * kBlockM + r) >> ps);                   // query row
@@ -970,6 +1036,30 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, const uint8_t* s
                 for (int i = 0; i < 8; ++i) w[i] = __float_as_uint(__uint_as_float(ov[8 * c + i]) * inv_l);
                 if (row_ok) ptx::st_global_v8(prow + 8 * c, w);
             }
+        } else if (stage) {
+            // Row r in the Q buffer's layout: 64-column boxes of 128-byte rows,
+            // 16-byte chunk k of row r at ((k ^ (r % 8)) * 16).
+            uint8_t* qt = smem_ptr + C::kQOff + ubuf * C::kTileBytes + r * 128;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float a = __uint_as_float(ov[32 * c + 2 * i]) * inv_l;
+                    const float b = __uint_as_float(ov[32 * c + 2 * i + 1]) * inv_l;
+                    w[i] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int g = 4 * c + i;                        // 16-byte chunk of the row
+                    *reinterpret_cast<uint4*>(qt + (g / 8) * C::kBoxBytes + (((g % 8) ^ (r & 7)) << 4)) =
+                        make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            ptx::fence_proxy_async_shared();                        // visible to the TMA store
+            __syncwarp();
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar(C::bOStaged + (int)(n_staged & 1u)));
+            ++n_staged;
         } else {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -1002,7 +1092,8 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, const uint8_t* s
 template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE, bool PACK>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                    const FwdParams p) {
     using C = TileCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     // Swizzled TMA tiles and the MMA descriptors both assume 1024-byte alignment.
@@ -1021,6 +1112,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t count = 1;
             if (i >= C::bQRdy && i < C::bQRdy + C::kQBufs) count = 2;
             if (i >= C::bTileEmpty && i < C::bTileEmpty + kTileSlots) count = tile_consumers(ROPE);
+            if (i >= C::bOStaged && i < C::bOStaged + 2) count = 4;
             ptx::mbar_init(bars + 8u * i, count);
         }
         *abort_flag = 0u;
@@ -1050,7 +1142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else if (warp == kTmaWarp)
             role_tma<D>(&tmK, &tmV, smem, smem_ptr, sc);
         else if (warp == kQWarp)
-            role_qload<D, CAUSAL, BF16, ROPE, PACK>(&tmQ, p, smem, smem_ptr, sc);
+            role_qload<D, CAUSAL, ADDITIVE, BF16, ROPE, PACK>(&tmQ, &tmO, p, smem, smem_ptr, sc);
         else if (ROPE && warp == kRopeWarp)
             role_rope_q<D, BF16>(p, smem, smem_ptr, sc);
         __syncwarp();

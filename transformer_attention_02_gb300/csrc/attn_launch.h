@@ -14,14 +14,15 @@ namespace attn {
 struct FwdParams;
 
 // Launches attn_fwd_kernel<D, CAUSAL, ADDITIVE, BF16, ROPE, PACK> with `grid`
-// persistent CTAs on `stream`. `attr_set` caches, per device, that the
+// CTAs on `stream` (tensor maps of Q, K, V and of the output O, which the
+// kernel stores through for the upper sub-tiles when it writes 16-bit O). `attr_set` caches, per device, that the
 // variant's shared-memory attribute has been set and its register count
 // checked (the in-kernel register split needs exactly the launch count).
 // Returns ATTN_OK, ATTN_ERR_UNSUPPORTED (register count differs) or
 // ATTN_ERR_CUDA.
 template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE, bool PACK>
 int launch_fwd(bool& attr_set, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-               const FwdParams& p, int grid, cudaStream_t stream);
+               const CUtensorMap& to, const FwdParams& p, int grid, cudaStream_t stream);
 
 // Process-unique id of the current CUDA context (the current device's primary
 // context is made current first when no context is). Per-context caches of the
