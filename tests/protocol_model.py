@@ -388,22 +388,22 @@ def role_qload(sim: Sim, tiles):
     uses = [0] * p.q_bufs
     nq = 0
     entries = ring_entries(tiles)
-    st = {"produced": 0, "clc": 0, "drained": False, "staged": 0}
-    staged = [None] * p.q_bufs          # (staging index, tile key) of the O a buffer will hold
+    st = {"produced": 0, "clc": 0, "drained": False, "staged": [0, 0]}
+    staged = [None] * p.q_bufs          # (warpgroup, its staging index, tile key) of the O a buffer will hold
 
     def store_staged(buf):
-        """Wait until warpgroup 1 has written the tile's O into buf, then copy it
-        out (the tensor store reads the buffer before this warp goes on). The
-        stagings alternate between two barriers: at most two are ever waiting
-        to be stored (the last two tiles' upper buffers), so no wait can fall
-        a whole phase behind."""
-        idx, key = staged[buf]
-        ok = yield ("wait", f"o_staged{idx % 2}", idx // 2)
+        """Wait until the warpgroup has written the tile's O into buf, then copy
+        it out (the tensor store reads the buffer before this warp goes on).
+        Each warpgroup's stagings alternate between two barriers of its own: at
+        most two of them are ever waiting to be stored, so no wait can fall a
+        whole phase behind."""
+        wg, idx, key = staged[buf]
+        ok = yield ("wait", f"o_staged{wg}{idx % 2}", idx // 2)
         if not ok:
             return False
 
-        def store(buf=buf, key=key):
-            sim.expect(f"q{buf}", ("O", key), f"store of the staged O of {key}")
+        def store(buf=buf, key=key, wg=wg):
+            sim.expect(f"q{buf}", ("O", key, wg), f"store of the staged O of {key}, sub-tile {wg}")
             sim.res[f"q{buf}"] = "free"
         yield ("act", store)
         staged[buf] = None
@@ -453,9 +453,9 @@ def role_qload(sim: Sim, tiles):
                 return False
         if staged[buf] is not None and not (yield from store_staged(buf)):
             return False
-        if p.stage_o and t == 1 and ti.nb[1] > 0:
-            staged[buf] = (st["staged"], _tile_key(ti))
-            st["staged"] += 1
+        if p.stage_o and ti.nb[t] > 0:
+            staged[buf] = (t, st["staged"][t], _tile_key(ti))
+            st["staged"][t] += 1
         yield ("expect_tx", f"q_full{buf}", 1)
         yield ("tma", f"q_full{buf}", 1, f"q{buf}", _q_tag(ti, t, p))
         uses[buf] += 1
@@ -504,7 +504,7 @@ def role_qload(sim: Sim, tiles):
             ti = tn
             have = more
     # the O of the last tiles still waits in their buffers (in staging order)
-    for buf in sorted((b for b in range(p.q_bufs) if staged[b] is not None), key=lambda b: staged[b][0]):
+    for buf in sorted((b for b in range(p.q_bufs) if staged[b] is not None), key=lambda b: staged[b][:2]):
         if not (yield from store_staged(buf)):
             break
     for b in range(p.q_bufs):
@@ -686,8 +686,8 @@ def role_mma(sim: Sim, tiles):
 
 def role_softmax(sim: Sim, tiles, t: int):
     """Softmax warpgroup t: per block, S_t -> P_t (rescaling O_t), then the
-    epilogue; warpgroup 1 writes its O into the upper sub-tile's Q buffer
-    (stage_o) and signals the Q warp, which stores it."""
+    epilogue; with stage_o it writes its O into its sub-tile's Q buffer and
+    signals the Q warp, which stores it."""
     p = sim.p
     s_cnt = 0
     o_cnt = 0
@@ -701,7 +701,7 @@ def role_softmax(sim: Sim, tiles, t: int):
         k += 1
         nb = ti.nb[t]
         key = _tile_key(ti)
-        ubuf = q_slot(nq, 1, p.q_bufs)[0]
+        qbuf = q_slot(nq, t, p.q_bufs)[0]
         if ti.n > 0:
             nq += 1
         if nb == 0:
@@ -732,20 +732,20 @@ def role_softmax(sim: Sim, tiles, t: int):
             sim.expect(f"O{t}", ("O", key, t, nb - 1), f"epilogue {t}")
             sim.res[f"O{t}"] = ("read", key, t)
         yield ("act", epi)
-        if p.stage_o and t == 1:
+        if p.stage_o:
             sidx = n_staged
             n_staged += 1
 
-            def stage(ti=ti, ubuf=ubuf):
-                q = sim.res.get(f"q{ubuf}")
-                if not (isinstance(q, tuple) and q[:4] == _q_tag(ti, 1, p)[:4]):
-                    raise ProtocolError(f"staging the O of {key} into q{ubuf}, which holds {q}")
-                if sim.reads_pending(f"q{ubuf}"):
-                    raise ProtocolError(f"staging the O of {key} into q{ubuf} while an MMA still reads it")
-                sim.res[f"q{ubuf}"] = ("O", key)
+            def stage(ti=ti, qbuf=qbuf):
+                q = sim.res.get(f"q{qbuf}")
+                if not (isinstance(q, tuple) and q[:4] == _q_tag(ti, t, p)[:4]):
+                    raise ProtocolError(f"staging the O of {key} into q{qbuf}, which holds {q}")
+                if sim.reads_pending(f"q{qbuf}"):
+                    raise ProtocolError(f"staging the O of {key} into q{qbuf} while an MMA still reads it")
+                sim.res[f"q{qbuf}"] = ("O", key, t)
             yield ("act", stage)
             for _ in range(4):                   # one arrival per warp, after its rows are written
-                yield ("arrive", f"o_staged{sidx % 2}")
+                yield ("arrive", f"o_staged{t}{sidx % 2}")
 
 
 # ---------------------------------------------------------------- scheduler
@@ -761,8 +761,9 @@ def make_sim(p: Params, seed: int, timeouts: bool = False):
         sim.bars[f"tile_full{i}"] = Barrier(f"tile_full{i}", 1)
         sim.bars[f"tile_empty{i}"] = Barrier(f"tile_empty{i}", p.tile_consumers)
     sim.bars["clc"] = Barrier("clc", 1)
-    for i in range(2):
-        sim.bars[f"o_staged{i}"] = Barrier(f"o_staged{i}", 4)
+    for t in range(2):
+        for i in range(2):
+            sim.bars[f"o_staged{t}{i}"] = Barrier(f"o_staged{t}{i}", 4)
     sim.bars["drain"] = Barrier("drain", 1)
     sim.bars["stall"] = Barrier("stall", 1)
     tiles = schedule(p)

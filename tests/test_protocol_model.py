@@ -154,7 +154,10 @@ MUTATIONS = {
     # the producer reads the launch-control response without waiting for it
     "clc_wait_skipped": ('            ok = yield ("wait", "clc", st["clc"])', '            ok = True'),
     # the Q warp stores a staged O without waiting for warpgroup 1 to write it
-    "stage_wait_skipped": ('ok = yield ("wait", f"o_staged{idx % 2}", idx // 2)', 'ok = True'),
+    "stage_wait_skipped": ('ok = yield ("wait", f"o_staged{wg}{idx % 2}", idx // 2)', 'ok = True'),
+    # the Q warp waits for the other warpgroup's staging
+    "stage_wrong_warpgroup": ('ok = yield ("wait", f"o_staged{wg}{idx % 2}", idx // 2)',
+                              'ok = yield ("wait", f"o_staged{1 - wg}{idx % 2}", idx // 2)'),
     # the Q warp reloads a buffer that still holds a staged O
     "stage_store_skipped": ("        if staged[buf] is not None and not (yield from store_staged(buf)):\n",
                             "        if False:\n"),

@@ -125,8 +125,8 @@ struct TileCfg {
     static constexpr int bTileFull = bQRdy + kQBufs;  // [kTileSlots] tile ring entry published
     static constexpr int bTileEmpty = bTileFull + kTileSlots;   // [kTileSlots] entry freed by every consumer
     static constexpr int bClc = bTileEmpty + kTileSlots;      // cluster-launch-control response landed
-    static constexpr int bOStaged = bClc + 1;         // [2] upper sub-tile's O staged (one arrival per warp)
-    static constexpr int kNumBars = bOStaged + 2;
+    static constexpr int bOStaged = bClc + 1;         // [2][2] sub-tile's O staged (one arrival per warp)
+    static constexpr int kNumBars = bOStaged + 4;
     // tile ring: kTileSlots entries of 32 bytes, read and written as 16-byte vectors
     static constexpr int kTileOff = (kBarOff + 8 * kNumBars + 31) / 32 * 32;
     static constexpr int kClcOff = kTileOff + kTileSlots * 32;   // 16-byte cluster-launch-control response
@@ -555,22 +555,23 @@ __device__ void role_qload(const CUtensorMap* tmQ, const CUtensorMap* tmO, const
 
     uint32_t uses[C::kQBufs] = {};              // loads issued into each buffer
     uint32_t nq = 0;                            // work tiles with at least one block
-    // Staged output (see role_softmax): a buffer that held an upper sub-tile
-    // with blocks receives that tile's O from warpgroup 1; before the buffer
-    // is loaded again this warp waits for it (bOStaged, alternating between
-    // two barriers: at most the last two tiles' stagings are ever pending) and
-    // stores it by TMA. The store has read the buffer when wait_group.read
-    // returns, so the next load may then overwrite it.
+    // Staged output (see role_softmax): a buffer that held a sub-tile with
+    // blocks receives that sub-tile's O from its warpgroup; before the buffer
+    // is loaded again this warp waits for it (bOStaged: each warpgroup's
+    // stagings alternate between two barriers of its own, and at most two of
+    // them are ever pending) and stores it by TMA. The store has read the
+    // buffer when wait_group.read returns, so the next load may then
+    // overwrite it.
     constexpr bool kStaging = kStagesO<D, ADDITIVE, PACK>();
     const bool stage_o = kStaging && p.o_part == nullptr;
     constexpr int kSt = kStaging ? C::kQBufs : 1;
-    int st_idx[kSt], st_b[kSt], st_h[kSt], st_m[kSt];
+    int st_idx[kSt], st_wg[kSt], st_b[kSt], st_h[kSt], st_m[kSt];
 #pragma unroll
-    for (int b = 0; b < kSt; ++b) st_idx[b] = st_b[b] = st_h[b] = st_m[b] = -1;
-    int n_staged = 0;
+    for (int b = 0; b < kSt; ++b) st_idx[b] = st_wg[b] = st_b[b] = st_h[b] = st_m[b] = -1;
+    int n_staged[2] = {0, 0};
     auto store_staged = [&](int buf) -> bool {
         const int idx = st_idx[buf];
-        if (!warp_wait(bar(C::bOStaged + (idx & 1)), ((uint32_t)idx >> 1) & 1u, sc)) return false;
+        if (!warp_wait(bar(C::bOStaged + 2 * st_wg[buf] + (idx & 1)), ((uint32_t)idx >> 1) & 1u, sc)) return false;
         if (leader) {
             for (int c = 0; c < C::kBoxes; ++c)
                 ptx::tma_store_4d(tmO, smem + C::kQOff + buf * C::kTileBytes + c * C::kBoxBytes, c * C::kBoxCols,
@@ -585,8 +586,9 @@ __device__ void role_qload(const CUtensorMap* tmQ, const CUtensorMap* tmO, const
     auto load = [&](int buf, int row0, const TileInfo& ti, bool upper) -> bool {
         if (uses[buf] > 0 && !warp_wait(bar(C::bQEmpty + buf), (uses[buf] - 1) & 1u, sc)) return false;
         if (kStaging && st_idx[buf] >= 0 && !store_staged(buf)) return false;
-        if (kStaging && stage_o && upper && ti.nb[1] > 0) {
-            st_idx[buf] = n_staged++;
+        if (kStaging && stage_o && ti.nb[upper ? 1 : 0] > 0) {
+            st_wg[buf] = upper ? 1 : 0;
+            st_idx[buf] = n_staged[upper ? 1 : 0]++;
             st_b[buf] = ti.b;
             st_h[buf] = ti.h;
             st_m[buf] = row0;
@@ -643,12 +645,14 @@ __device__ void role_qload(const CUtensorMap* tmQ, const CUtensorMap* tmO, const
         }
     }
     if constexpr (kStaging) {
-        // The last tiles' staged O (at most two buffers), in staging order.
-        for (int pass = 0; pass < 2; ++pass) {
+        // The last tiles' staged O, each warpgroup's in staging order.
+        for (int pass = 0; pass < C::kQBufs; ++pass) {
             int next = -1;
 #pragma unroll
             for (int b = 0; b < C::kQBufs; ++b)
-                if (st_idx[b] >= 0 && (next < 0 || st_idx[b] < st_idx[next])) next = b;
+                if (st_idx[b] >= 0 && (next < 0 || st_wg[b] < st_wg[next] ||
+                                       (st_wg[b] == st_wg[next] && st_idx[b] < st_idx[next])))
+                    next = b;
             if (next < 0 || !store_staged(next)) break;
         }
         if (leader) ptx::bulk_wait_group<0>();    // every store issued here has completed
@@ -828,14 +832,14 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint8_t* smem_pt
     constexpr float kLn2 = 0.6931471805599453f;
     constexpr float kLog2e = 1.4426950408889634f;
     uint32_t s_phase = 0, o_phase = 0;
-    // With an additive mask and D = 128, warpgroup 1 (16-bit output, no split
-    // keys, no head packing) writes its O into the upper sub-tile's Q buffer,
-    // free once "O ready" has arrived, and the Q warp stores it by TMA
-    // (role_qload): its epilogue then skips the row-strided global stores,
-    // which compete with the mask rows' loads for the L1 (those loads bound
-    // the masked kernel). Without a mask, or at D = 64, the direct stores are
-    // as fast or faster.
-    const bool stage = kStagesO<D, ADDITIVE, PACK>() && wg == 1 && p.o_part == nullptr;
+    // With an additive mask and D = 128 (16-bit output, no split keys, no head
+    // packing), each warpgroup writes its O into its sub-tile's Q buffer, free
+    // once "O ready" has arrived, and the Q warp stores it by TMA (role_qload):
+    // the epilogue then skips the row-strided global stores, which compete
+    // with the mask rows' loads for the L1 (those loads bound the masked
+    // kernel). Without a mask, or at D = 64, the direct stores are as fast or
+    // faster.
+    const bool stage = kStagesO<D, ADDITIVE, PACK>() && p.o_part == nullptr;
     uint32_t nq = 0, n_staged = 0;                            // tiles with blocks; O staged so far
 
     const uint8_t* ring = smem_ptr + C::kTileOff;
@@ -844,7 +848,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint8_t* smem_pt
         if (!fetch_tile_warp(bar(C::bTileFull), bar(C::bTileEmpty), ring, k, ti, sc)) return;
         if (ti.n < 0) break;                                  // end marker
         uint32_t use_unused;
-        const uint32_t ubuf = q_slot(nq, 1, use_unused);      // this tile's upper Q buffer
+        const uint32_t qbuf = q_slot(nq, wg, use_unused);     // this sub-tile's Q buffer
         if (ti.n > 0) ++nq;
         const int nb = ti.nb[wg];
         const int ps = PACK ? p.pack_shift : 0;
@@ -1039,7 +1043,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint8_t* smem_pt
         } else if (stage) {
             // Row r in the Q buffer's layout: 64-column boxes of 128-byte rows,
             // 16-byte chunk k of row r at ((k ^ (r % 8)) * 16).
-            uint8_t* qt = smem_ptr + C::kQOff + ubuf * C::kTileBytes + r * 128;
+            uint8_t* qt = smem_ptr + C::kQOff + qbuf * C::kTileBytes + r * 128;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t w[16];
@@ -1058,7 +1062,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint8_t* smem_pt
             }
             ptx::fence_proxy_async_shared();                        // visible to the TMA store
             __syncwarp();
-            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar(C::bOStaged + (int)(n_staged & 1u)));
+            if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar(C::bOStaged + 2 * wg + (int)(n_staged & 1u)));
             ++n_staged;
         } else {
 #pragma unroll
@@ -1112,7 +1116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t count = 1;
             if (i >= C::bQRdy && i < C::bQRdy + C::kQBufs) count = 2;
             if (i >= C::bTileEmpty && i < C::bTileEmpty + kTileSlots) count = tile_consumers(ROPE);
-            if (i >= C::bOStaged && i < C::bOStaged + 2) count = 4;
+            if (i >= C::bOStaged && i < C::bOStaged + 4) count = 4;
             ptx::mbar_init(bars + 8u * i, count);
         }
         *abort_flag = 0u;
