@@ -906,7 +906,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint8_t* smem_pt
                     const float4* m4 = reinterpret_cast<const float4*>(mrow + key0);
 #pragma unroll
                     for (int c = 0; c < kBlockN / 4; ++c) {
-                        const float4 mv = __ldg(m4 + c);
+                        const float4 mv = ptx::ld_global_nc_v4(reinterpret_cast<const float*>(m4 + c));
                         x[4 * c + 0] = mv.x;
                         x[4 * c + 1] = mv.y;
                         x[4 * c + 2] = mv.z;

@@ -300,11 +300,22 @@ __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r) {
                  : "memory");
 }
 
-// 32-byte read-only vector load from global memory (the address must be 32-byte aligned).
+// 32-byte read-only vector load from global memory (the address must be 32-byte
+// aligned) that does not allocate in L1: the additive mask is read once per
+// (row, block) from L2, and its lines would only evict each other in L1.
 __device__ __forceinline__ void ld_global_nc_v8(const float* ptr, float* r) {
-    asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+    asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
                  : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7])
                  : "l"(ptr));
+}
+
+// 16-byte read-only load that does not allocate in L1 (as above).
+__device__ __forceinline__ float4 ld_global_nc_v4(const float* ptr) {
+    float4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(ptr));
+    return r;
 }
 
 // Per-warpgroup register budget (all four warps of a warpgroup execute it).
