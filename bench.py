@@ -508,6 +508,11 @@ def run_ours(args, cfg):
         "wall_s_timed_region": t_wall1 - t_wall0,
         "kernel_source_hash": kernel_source_hash(),
     }
+    if cfg.additive_mask:
+        # The tensor roofline is the nominal one; what the masked kernel actually
+        # hits (ncu) is the L1 throughput of the FP32 mask rows, one row per
+        # thread.
+        line["roofline"]["limiter"] = "L1 throughput of the FP32 mask-row loads (32 rows per warp request)"
     if extra:
         line["configs"] = extra
     if args.rope:
