@@ -37,6 +37,7 @@ SMALL = [
     (1, 2, 2, 64, 2000, 128, 0),
     (3, 6, 3, 640, 640, 64, 0),
     (1, 4, 4, 700, 700, 128, 3),
+    (2, 3, 3, 1000, 900, 128, 2),         # additive, several tiles per CTA; staged O with a ragged tail
 ]
 
 

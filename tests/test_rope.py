@@ -79,6 +79,7 @@ CASES = [
     (1, 4, 1, 1, 3000, 128, 1, 2999, 0, 0, "bf16"),      # MQA decode, automatic split
     (2, 4, 2, 130, 520, 64, 0, 5, 3, 1, "f16"),          # no mask, offsets, fp16, D = 64
     (1, 2, 2, 100, 260, 128, 3, 160, 0, 1, "bf16"),      # causal + additive mask
+    (1, 2, 2, 600, 600, 128, 2, 0, 0, 1, "f16"),         # additive mask: both sub-tiles' O staged, ragged tail
     (1, 8, 8, 600, 600, 64, 1, 0, 0, 1, "bf16"),
     (2, 16, 4, 8, 2048, 128, 1, 2040, 0, 4, "f16"),      # short prefill over a cache, four ranges
 ]
