@@ -12,16 +12,22 @@
 //
 // Work decomposition ("ops-transformer：…实战" §3.2 and §5.2: B and H are
 // independent, the sequence is split into blocks, all cores kept busy):
-// a work tile is (b, h, 256 query rows). A persistent grid of one CTA per SM
-// walks the tiles; with a causal mask the longest tiles come first and the
-// query heads that share a K/V head are adjacent so their K/V stay in L2.
+// a work tile is (b, h, 256 query rows). The grid has one CTA per tile; at
+// most one fits on an SM, and a running CTA takes over the tiles of CTAs that
+// have not started (cluster launch control), so the grid behaves as a
+// persistent one with a dynamic schedule. With a causal mask the longest tiles
+// come first and the query heads that share a K/V head are grouped so that
+// their K/V stay in L2 (tile_info).
 //
 // Roles inside a CTA (384 threads):
 //   warps 0-3  softmax warpgroup 0: query rows [m0, m0+128)      (TMEM lanes 0-127)
 //   warps 4-7  softmax warpgroup 1: query rows [m0+128, m0+256)
 //   warp  8    MMA issuer (one thread) + TMEM allocation
 //   warp  9    TMA producer of K/V (one thread) + barrier initialisation
-//   warp 10    TMA producer of Q (one thread), a tile ahead for the lower sub-tile
+//   warp 10    producer of the shared-memory tile ring (the CTA's work tiles)
+//              and TMA producer of Q, a tile ahead for the lower sub-tile; in
+//              the D=128 masked variants it also stores the output staged in
+//              the Q buffers
 //   warp 11    idle (it completes the third warpgroup for the register split);
 //              in the rotary variant it rotates half of each Q sub-tile
 // Pipelining ("ops-transformer：…实战" §2.3): while one warpgroup exponentiates
