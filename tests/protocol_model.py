@@ -2,9 +2,9 @@
 
 The fused kernel (transformer_attention_02_gb300/csrc/attn_kernel.cuh) runs
 five roles in one CTA that hand work to each other through shared-memory
-mbarriers: the K/V TMA producer, the Q TMA producer (and, in the rotary
-variant, a second rotating warp), the single-thread MMA issuer and two softmax
-warpgroups. This module re-states each role's control flow in Python, over the
+mbarriers: the K/V TMA producer, the Q TMA producer, the single-thread MMA
+issuer, two softmax warpgroups and, in the rotary variant, four warps that
+rotate the Q sub-tiles. This module re-states each role's control flow in Python, over the
 same tile schedule, and runs the roles under an adversarial scheduler together
 with the asynchronous agents they drive (TMA copies that land in any order,
 the tensor core's in-order queue of MMAs and commits).
@@ -58,7 +58,7 @@ class Params:
     Sq: int = 512
     Sk: int = 512
     num_splits: int = 1          # key ranges (split-key mode when > 1)
-    rope: bool = False           # rotary variant: Q rotated by two warps, "Q ready" has two arrivals
+    rope: bool = False           # rotary variant: Q rotated by four warps, "Q ready" has four arrivals
     additive: bool = False       # additive-mask variant: warpgroup 1's O leaves through its Q buffer
     pack_shift: int = 0          # GQA head packing: 2^pack_shift query heads share a tile's rows
     grid: int = 1                # persistent CTAs
@@ -72,8 +72,9 @@ class Params:
     @property
     def tile_consumers(self) -> int:
         """Arrivals that free a tile-ring entry: the K/V producer, the MMA
-        issuer, the eight softmax warps and, in the rotary variant, warp 11."""
-        return 1 + 1 + 8 + (1 if self.rope else 0)
+        issuer, the eight softmax warps and, in the rotary variant, the four
+        rotating warps."""
+        return 1 + 1 + 8 + (4 if self.rope else 0)
 
     @property
     def slots(self) -> int:
@@ -368,7 +369,7 @@ def _q_tag(ti: Tile, t: int, p: Params):
     return ("Q", ti.b, ti.h, ti.m0 + t * (BLOCK_M >> p.pack_shift))
 
 
-def _rotate(sim: Sim, buf: int, half: int):
+def _rotate(sim: Sim, buf: int, quarter: int):
     def fn():
         name = f"q{buf}"
         st = sim.res.get(name)
@@ -376,14 +377,16 @@ def _rotate(sim: Sim, buf: int, half: int):
             raise ProtocolError(f"rotation of {name} before its copy landed ({st})")
         if sim.reads_pending(name):
             raise ProtocolError(f"rotation of {name} while an MMA reads it")
-        sim.res[name] = st + (("rot", half),)
+        if ("rot", quarter) in st[4:]:
+            raise ProtocolError(f"rows of quarter {quarter} of {name} rotated twice ({st})")
+        sim.res[name] = st + (("rot", quarter),)
     return ("act", fn)
 
 
 def role_qload(sim: Sim, tiles):
     """Q producer (warp 10) and producer of the tile ring: each entry is
     published when this warp is about to load that tile's Q (next_work of the
-    kernel); in the rotary variant it also rotates rows 0-63."""
+    kernel)."""
     p = sim.p
     uses = [0] * p.q_bufs
     nq = 0
@@ -461,48 +464,14 @@ def role_qload(sim: Sim, tiles):
         uses[buf] += 1
         return True
 
-    def rotate(buf):
-        ok = yield ("wait", f"q_full{buf}", uses[buf] - 1)     # its latest load
-        if not ok:
-            return False
-        yield _rotate(sim, buf, 0)
-        yield ("arrive", f"q_rdy{buf}")
-        return True
-
-    if not p.rope:
-        while True:
-            r, ti = yield from next_work()
-            if r <= 0:
-                break
-            lb, ub = q_bufs_of(nq, p.q_bufs)
-            if not (yield from load(lb, ti, 0)) or not (yield from load(ub, ti, 1)):
-                break
-            nq += 1
-    else:
+    while True:
         r, ti = yield from next_work()
-        have = r > 0 and (yield from load(q_bufs_of(0, p.q_bufs)[0], ti, 0))
-        lower_rotated = False
-        while have:
-            b0, b1 = q_bufs_of(nq, p.q_bufs)
-            if not (yield from load(b1, ti, 1)):
-                break
-            if not lower_rotated and not (yield from rotate(b0)):
-                break
-            if not (yield from rotate(b1)):
-                break
-            rn, tn = yield from next_work()
-            if rn < 0:
-                break
-            more = rn > 0
-            nb0 = q_bufs_of(nq + 1, p.q_bufs)[0]
-            if more and not (yield from load(nb0, tn, 0)):
-                break
-            if more and not (yield from rotate(nb0)):
-                break
-            lower_rotated = True
-            nq += 1
-            ti = tn
-            have = more
+        if r <= 0:
+            break
+        lb, ub = q_bufs_of(nq, p.q_bufs)
+        if not (yield from load(lb, ti, 0)) or not (yield from load(ub, ti, 1)):
+            break
+        nq += 1
     # the O of the last tiles still waits in their buffers (in staging order)
     for buf in sorted((b for b in range(p.q_bufs) if staged[b] is not None), key=lambda b: staged[b][:2]):
         if not (yield from store_staged(buf)):
@@ -512,8 +481,8 @@ def role_qload(sim: Sim, tiles):
             yield ("drain", f"q_full{b}", uses[b] - 1)
 
 
-def role_rope_q(sim: Sim, tiles):
-    """Rotary variant, warp 11: rotates rows 64-127 of every Q sub-tile."""
+def role_rope_q(sim: Sim, tiles, quarter: int):
+    """Rotary variant, warp 12 + quarter: rotates its 32 rows of every Q sub-tile."""
     p = sim.p
     nq = 0
     k = 0
@@ -529,7 +498,7 @@ def role_rope_q(sim: Sim, tiles):
             ok = yield ("wait", f"q_full{buf}", use)
             if not ok:
                 return
-            yield _rotate(sim, buf, 1)
+            yield _rotate(sim, buf, quarter)
             yield ("arrive", f"q_rdy{buf}")
         nq += 1
 
@@ -540,7 +509,7 @@ def _qk(sim: Sim, ti: Tile, t: int, q_buf: int, k_slot: int, blk: int):
     key = _tile_key(ti)
     q_tag = _q_tag(ti, t, p)
     if p.rope:
-        q_tag = q_tag + (("rot", 0), ("rot", 1))
+        q_tag = q_tag + tuple(("rot", i) for i in range(4))
     k_tag = ("KV", 0, ti.b, ti.hk, ti.kb0 + blk)
 
     def fn():
@@ -753,7 +722,7 @@ def role_softmax(sim: Sim, tiles, t: int):
 def make_sim(p: Params, seed: int, timeouts: bool = False):
     sim = Sim(p, random.Random(seed), timeouts=timeouts)
     names = [("q_full", p.q_bufs, 1), ("q_empty", p.q_bufs, 1), ("s_full", 2, 1), ("p_full", 2, 1),
-             ("o_full", 2, 1), ("kv_full", p.slots, 1), ("kv_empty", p.slots, 1), ("q_rdy", p.q_bufs, 2)]
+             ("o_full", 2, 1), ("kv_full", p.slots, 1), ("kv_empty", p.slots, 1), ("q_rdy", p.q_bufs, 4)]
     for base, n, count in names:
         for i in range(n):
             sim.bars[f"{base}{i}"] = Barrier(f"{base}{i}", count)
@@ -771,7 +740,7 @@ def make_sim(p: Params, seed: int, timeouts: bool = False):
              Proc("mma", role_mma(sim, tiles)), Proc("softmax0", role_softmax(sim, tiles, 0)),
              Proc("softmax1", role_softmax(sim, tiles, 1))]
     if p.rope:
-        procs.append(Proc("rope_q", role_rope_q(sim, tiles)))
+        procs += [Proc(f"rope_q{i}", role_rope_q(sim, tiles, i)) for i in range(4)]
     return sim, procs, tiles
 
 

@@ -1,12 +1,12 @@
 """The attention kernel's barrier protocol, checked on the CPU.
 
 tests/protocol_model.py re-states every role of the kernel (K/V and Q
-producers, the rotating warp of the rotary variant, the MMA issuer, the two
-softmax warpgroups) and runs them under many adversarial schedules together
-with the asynchronous TMA copies and the tensor core's in-order MMA queue. The
-cases cover both head dimensions (ring of 4 and 8 slots), causal and
+producers, the MMA issuer, the two softmax warpgroups, the four rotating
+warps of the rotary variant) and runs them under many adversarial schedules
+together with the asynchronous TMA copies and the tensor core's in-order MMA
+queue. The cases cover both head dimensions (ring of 4 and 8 slots), causal and
 non-causal tiles with ragged tails and Sq != Sk, sub-tiles with no key block,
-GQA head packing, split-key mode, the rotary variant's two-arrival "Q ready"
+GQA head packing, split-key mode, the rotary variant's four-arrival "Q ready"
 barriers, the additive-mask variant's output staged in a Q buffer and stored
 by the Q warp, and the abort path (a stalled wait that runs out; an abort raised at
 an arbitrary moment). Planted protocol mistakes must each be caught.
@@ -32,7 +32,7 @@ CASES = [
     M.Params(num_splits=3, Sq=100, Sk=1500, grid=2, cta=1),            # split keys
     M.Params(num_splits=4, Sq=1, Sk=2000, Hq=8, Hkv=2, pack_shift=2, grid=2, cta=0),   # packed decode
     M.Params(Hq=8, Hkv=2, pack_shift=2, Sq=40, Sk=900),
-    M.Params(rope=True),                                               # two-arrival "Q ready"
+    M.Params(rope=True),                                               # four-arrival "Q ready"
     M.Params(rope=True, D=64, causal=False, Sq=600, Sk=500),
     M.Params(rope=True, B=2, Hq=2, Hkv=1, Sq=700, Sk=700, grid=2, cta=1),
     M.Params(Sq=128, Sk=128, Hq=1, Hkv=1),                             # one block per tile
@@ -138,8 +138,11 @@ MUTATIONS = {
     # the softmax does not wait for S
     "softmax_skips_s_wait": ('            landed = yield ("wait", f"s_full{t}", s_cnt)',
                              '            landed = True'),
-    # "Q ready" of the rotary variant with one arrival instead of two
-    "rope_ready_one_arrival": ('("q_rdy", p.q_bufs, 2)', '("q_rdy", p.q_bufs, 1)'),
+    # "Q ready" of the rotary variant with three arrivals instead of four
+    "rope_ready_one_arrival": ('("q_rdy", p.q_bufs, 4)', '("q_rdy", p.q_bufs, 3)'),
+    # a rotating warp rotates the buffer before its copy has landed
+    "rope_skips_q_wait": ('            ok = yield ("wait", f"q_full{buf}", use)\n            if not ok:\n                return\n            yield _rotate(sim, buf, quarter)',
+                          '            ok = True\n            yield _rotate(sim, buf, quarter)'),
     # the softmax counts its S phases per tile instead of continuously
     "softmax_phase_reset": ("        ok = True\n        for j in range(nb):", "        ok = True\n        s_cnt = 0\n        for j in range(nb):"),
     # the issuer waits for Q of the upper sub-tile on the lower sub-tile's buffer
@@ -148,7 +151,7 @@ MUTATIONS = {
     # the tile-ring producer overwrites entries without waiting for them to be freed
     "ring_producer_skips_wait": ("    if k >= p.tile_slots:\n", "    if False:\n"),
     # one arrival too few frees a tile-ring entry (a consumer not counted)
-    "ring_consumer_undercount": ("        return 1 + 1 + 8 + (1 if self.rope else 0)", "        return 1 + 8 + (1 if self.rope else 0)"),
+    "ring_consumer_undercount": ("        return 1 + 1 + 8 + (4 if self.rope else 0)", "        return 1 + 8 + (4 if self.rope else 0)"),
     # the producer leaves without waiting for a launch-control response in flight
     "clc_drain_skipped": ('                yield ("drain", "clc", st["clc"])       # the response must land before the CTA exits\n', ""),
     # the producer reads the launch-control response without waiting for it

@@ -15,15 +15,15 @@ int launch_fwd(bool& attr_set, const CUtensorMap& tq, const CUtensorMap& tk, con
     auto kernel = attn_fwd_kernel<D, CAUSAL, ADDITIVE, BF16, ROPE, PACK>;
     constexpr int smem = TileCfg<D>::kSmemBytes;
     if (!attr_set) {
-        // The in-kernel register split assumes exactly kLaunchRegs per thread at launch.
+        // The in-kernel register split assumes exactly launch_regs(ROPE) per thread at launch.
         cudaFuncAttributes fa{};
         if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return ATTN_ERR_CUDA;
-        if (fa.numRegs != kLaunchRegs) return ATTN_ERR_UNSUPPORTED;
+        if (fa.numRegs != launch_regs(ROPE)) return ATTN_ERR_UNSUPPORTED;
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return ATTN_ERR_CUDA;
         attr_set = true;
     }
-    kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, to, p);
+    kernel<<<grid, kernel_threads(ROPE), smem, stream>>>(tq, tk, tv, to, p);
     return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

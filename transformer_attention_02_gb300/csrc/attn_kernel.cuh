@@ -19,7 +19,7 @@
 // come first and the query heads that share a K/V head are grouped so that
 // their K/V stay in L2 (tile_info).
 //
-// Roles inside a CTA (384 threads):
+// Roles inside a CTA (384 threads; 512 in the rotary variant):
 //   warps 0-3  softmax warpgroup 0: query rows [m0, m0+128)      (TMEM lanes 0-127)
 //   warps 4-7  softmax warpgroup 1: query rows [m0+128, m0+256)
 //   warp  8    MMA issuer (one thread) + TMEM allocation
@@ -28,8 +28,9 @@
 //              and TMA producer of Q, a tile ahead for the lower sub-tile; in
 //              the D=128 masked variants it also stores the output staged in
 //              the Q buffers
-//   warp 11    idle (it completes the third warpgroup for the register split);
-//              in the rotary variant it rotates half of each Q sub-tile
+//   warp 11    idle (it completes the third warpgroup for the register split)
+//   warps 12-15 rotary variant only: rotate each Q sub-tile as it lands, 32
+//              rows per warp
 // Pipelining ("ops-transformer：…实战" §2.3): while one warpgroup exponentiates
 // its scores, the tensor cores work on the other warpgroup's tile, and the TMA
 // warp streams the next K/V tiles into a ring of shared-memory slots.
@@ -80,27 +81,35 @@ static_assert(sizeof(FwdParams) <= 128, "FwdParams size");
 constexpr int kFlagOVec8 = 1;         // O rows may be written with 32-byte stores
 constexpr int kFlagDebugStall = 2;    // the MMA issuer waits on a barrier nothing signals (timeout test)
 
-constexpr int kThreads = 384;               // three warpgroups
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
 constexpr int kQWarp = 10;
-constexpr int kRopeWarp = 11;               // second rotating warp of the rotary variant
-// Register split: launched at 168 per thread (384 x 168 = 64512), then the
-// softmax warpgroups grow to 192 and the MMA/TMA warpgroup shrinks to 120:
-// 128 x (192 + 192 + 120) = 64512. The host refuses to launch unless the
-// compiled kernel uses exactly kLaunchRegs, so the split always fits.
-constexpr int kLaunchRegs = 168;
-constexpr uint32_t kSoftmaxRegs = 192;
-constexpr uint32_t kControlRegs = 120;
-static_assert(128 * (2 * kSoftmaxRegs + kControlRegs) <= kThreads * kLaunchRegs, "register split");
+constexpr int kRotateWarp0 = 12;            // rotary variant: warps 12-15 rotate the Q sub-tiles
+// Threads and register split. Three warpgroups (four in the rotary variant),
+// launched at 168 registers per thread (384 x 168 = 64512), then the softmax
+// warpgroups grow to 192 and the MMA/TMA/Q warpgroup shrinks to 120:
+// 128 x (192 + 192 + 120) = 64512. Rotary variant: launched at 128
+// (512 x 128 = 65536), softmax 184, MMA/TMA/Q 96, rotation 48:
+// 128 x (184 + 184 + 96 + 48) = 65536. The host refuses to launch unless the
+// compiled kernel uses exactly launch_regs(ROPE), so the split always fits.
+__host__ __device__ constexpr int kernel_threads(bool rope) { return rope ? 512 : 384; }
+__host__ __device__ constexpr int launch_regs(bool rope) { return rope ? 128 : 168; }
+__host__ __device__ constexpr uint32_t softmax_regs(bool rope) { return rope ? 184u : 192u; }
+__host__ __device__ constexpr uint32_t control_regs(bool rope) { return rope ? 96u : 120u; }
+constexpr uint32_t kRotateRegs = 48;
+static_assert(128 * (2 * softmax_regs(false) + control_regs(false)) <= kernel_threads(false) * launch_regs(false),
+              "register split");
+static_assert(128 * (2 * softmax_regs(true) + control_regs(true) + kRotateRegs) <=
+                  kernel_threads(true) * launch_regs(true),
+              "register split (rotary variant)");
 constexpr int kBlockM = 128;        // query rows per softmax warpgroup
 constexpr int kBlockN = 128;        // keys per K/V tile
 constexpr int kRowsPerTile = 2 * kBlockM;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: rescale O only when the max grows by > 2^8
 constexpr int kTileSlots = 8;               // entries of the shared-memory tile ring
 // Arrivals that free a tile-ring entry: the K/V producer, the MMA issuer, the
-// eight softmax warps and, in the rotary variant, warp 11.
-__host__ __device__ constexpr uint32_t tile_consumers(bool rope) { return 1 + 1 + 8 + (rope ? 1u : 0u); }
+// eight softmax warps and, in the rotary variant, the four rotating warps.
+__host__ __device__ constexpr uint32_t tile_consumers(bool rope) { return 1 + 1 + 8 + (rope ? 4u : 0u); }
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 constexpr unsigned int kStatusTimeout = 1u;
 
@@ -127,7 +136,7 @@ struct TileCfg {
     static constexpr int bStall = bDrain + 1;
     static constexpr int bKVFull = bStall + 1;        // [kSlots]
     static constexpr int bKVEmpty = bKVFull + kSlots;
-    static constexpr int bQRdy = bKVEmpty + kSlots;   // [kQBufs] rotary variant: Q rotated (two arrivals)
+    static constexpr int bQRdy = bKVEmpty + kSlots;   // [kQBufs] rotary variant: Q rotated (four arrivals)
     static constexpr int bTileFull = bQRdy + kQBufs;  // [kTileSlots] tile ring entry published
     static constexpr int bTileEmpty = bTileFull + kTileSlots;   // [kTileSlots] entry freed by every consumer
     static constexpr int bClc = bTileEmpty + kTileSlots;      // cluster-launch-control response landed
@@ -273,9 +282,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const S
 // off every other role's path, the MMA issuer's above all) and publishes it in
 // a ring of kTileSlots shared-memory entries of 32 bytes: tile_full[slot]
 // completes when the entry is written; every consumer (the K/V producer, the
-// MMA issuer, each softmax warp and, in the rotary variant, warp 11) copies the
-// entry and frees it at once with one arrival on tile_empty[slot]. After the
-// last tile the producer publishes an end marker (nb = -1).
+// MMA issuer, each softmax warp and, in the rotary variant, each rotating
+// warp) copies the entry and frees it at once with one arrival on
+// tile_empty[slot]. After the last tile the producer publishes an end marker
+// (nb = -1).
 __device__ __forceinline__ void store_tile_entry(uint8_t* entry, const TileInfo& t) {
     int4* e = reinterpret_cast<int4*>(entry);
     e[0] = make_int4(t.b, t.h, t.hk, t.m0);
@@ -448,13 +458,15 @@ __device__ __forceinline__ uint32_t q_slot(uint32_t nq, int t, uint32_t& use) {
     return i - 3u * use;
 }
 
-// Rotary variant, warp 11: rotates rows 64..127 of every Q sub-tile once its
-// load has landed (the Q warp does rows 0..63), in the order the Q warp loads
-// them, and signals "Q ready" (two arrivals per use).
+// Rotary variant, warps 12-15: warp 12 + q rotates rows 32q .. 32q+31 of every
+// Q sub-tile once its load has landed, in the order the Q warp loads them, and
+// signals "Q ready" (four arrivals per use). The four warps sit on the four
+// SM sub-partitions, so each shares its issue slots with two softmax warps.
 template <int D, bool BF16>
 __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr, const SyncCtx& sc) {
     using C = TileCfg<D>;
     const bool leader = (threadIdx.x & 31) == 0;
+    const int r0 = ((threadIdx.x >> 5) & 3) * 32;
     const uint32_t bars = smem + C::kBarOff;
     auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
     const uint8_t* ring = smem_ptr + C::kTileOff;
@@ -467,7 +479,7 @@ __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr
             uint32_t use;
             const uint32_t buf = q_slot(nq, t, use);
             if (!warp_wait(bar(C::bQFull + buf), use & 1u, sc)) return;
-            rope_rotate_rows<D, BF16>(smem_ptr + C::kQOff + buf * C::kTileBytes, kBlockM / 2, kBlockM,
+            rope_rotate_rows<D, BF16>(smem_ptr + C::kQOff + buf * C::kTileBytes, r0, r0 + 32,
                                       ti.m0 + t * kBlockM, p);
             if (leader) ptx::mbar_arrive(bar(C::bQRdy + buf));
         }
@@ -484,8 +496,8 @@ __device__ void role_rope_q(const FwdParams& p, uint32_t smem, uint8_t* smem_ptr
 // after this warp has loaded Q for it. The sub-tiles take the Q buffers in turn
 // (q_slot): the next tile's lower sub-tile is fetched as soon as the previous
 // tile's upper one is done, and its upper sub-tile while the current tile's
-// last key block runs. In the rotary variant this warp also rotates rows 0..63
-// of each sub-tile after it lands.
+// last key block runs. (In the rotary variant warps 12-15 rotate each
+// sub-tile after it lands.)
 template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE, bool PACK>
 __device__ void role_qload(const CUtensorMap* tmQ, const CUtensorMap* tmO, const FwdParams& p, uint32_t smem,
                            uint8_t* smem_ptr, const SyncCtx& sc) {
@@ -608,47 +620,13 @@ __device__ void role_qload(const CUtensorMap* tmQ, const CUtensorMap* tmO, const
         ++uses[buf];
         return true;
     };
-    auto rotate = [&](int buf, int row0) -> bool {      // the buffer's latest load
-        if (!warp_wait(bar(C::bQFull + buf), (uses[buf] - 1) & 1u, sc)) return false;
-        rope_rotate_rows<D, BF16>(smem_ptr + C::kQOff + buf * C::kTileBytes, 0, kBlockM / 2, row0, p);
-        if (leader) ptx::mbar_arrive(bar(C::bQRdy + buf));
-        return true;
-    };
-    if (!ROPE) {
-        TileInfo ti;
-        while (next_work(ti) > 0) {
-            uint32_t use;
-            const int b0 = (int)q_slot(nq, 0, use), b1 = (int)q_slot(nq, 1, use);
-            if (!load(b0, ti.m0, ti, false) || !load(b1, ti.m0 + (kBlockM >> (PACK ? p.pack_shift : 0)), ti, true))
-                break;
-            ++nq;
-        }
-    } else {
-        // The upper sub-tile of tile T is loaded as soon as its buffer is free
-        // and rotated as soon as it lands; then the next tile is assigned and
-        // its lower sub-tile loaded and rotated, a whole tile ahead of its use.
-        TileInfo ti, tn;
+    TileInfo ti;
+    while (next_work(ti) > 0) {
         uint32_t use;
-        bool have = next_work(ti) > 0 && load((int)q_slot(0, 0, use), ti.m0, ti, false);
-        bool lower_rotated = false;
-        while (have) {
-            const int b0 = (int)q_slot(nq, 0, use), b1 = (int)q_slot(nq, 1, use);
-            if (!load(b1, ti.m0 + kBlockM, ti, true)) break;
-            if (!lower_rotated && !rotate(b0, ti.m0)) break;
-            if (!rotate(b1, ti.m0 + kBlockM)) break;
-            // The next tile is taken over only now: this tile's upper sub-tile,
-            // which the MMA issuer needs first, is not held up by that request.
-            const int rn = next_work(tn);
-            if (rn < 0) break;
-            const bool more = rn > 0;
-            const int nb0 = (int)q_slot(nq + 1, 0, use);
-            if (more && !load(nb0, tn.m0, tn, false)) break;
-            if (more && !rotate(nb0, tn.m0)) break;
-            lower_rotated = true;
-            ++nq;
-            ti = tn;
-            have = more;
-        }
+        const int b0 = (int)q_slot(nq, 0, use), b1 = (int)q_slot(nq, 1, use);
+        if (!load(b0, ti.m0, ti, false) || !load(b1, ti.m0 + (kBlockM >> (PACK ? p.pack_shift : 0)), ti, true))
+            break;
+        ++nq;
     }
     if constexpr (kStaging) {
         // The last tiles' staged O, each warpgroup's in staging order.
@@ -1100,7 +1078,7 @@ __device__ void role_softmax(const FwdParams& p, uint32_t smem, uint8_t* smem_pt
 
 // ------------------------------------------------------------------ kernel
 template <int D, bool CAUSAL, bool ADDITIVE, bool BF16, bool ROPE, bool PACK>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kernel_threads(ROPE), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
                     const FwdParams p) {
@@ -1120,7 +1098,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bars = smem + C::kBarOff;
         for (int i = 0; i < C::kNumBars; ++i) {
             uint32_t count = 1;
-            if (i >= C::bQRdy && i < C::bQRdy + C::kQBufs) count = 2;
+            if (i >= C::bQRdy && i < C::bQRdy + C::kQBufs) count = 4;
             if (i >= C::bTileEmpty && i < C::bTileEmpty + kTileSlots) count = tile_consumers(ROPE);
             if (i >= C::bOStaged && i < C::bOStaged + 4) count = 4;
             ptx::mbar_init(bars + 8u * i, count);
@@ -1143,18 +1121,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const SyncCtx sc{abort_flag, p.status, p.timeout_ns};
 
     if (warp < 8) {
-        ptx::setmaxnreg_inc<kSoftmaxRegs>();
+        ptx::setmaxnreg_inc<softmax_regs(ROPE)>();
         role_softmax<D, CAUSAL, ADDITIVE, BF16, PACK>(p, smem, smem_ptr, tmem, warp >> 2, sc);
-    } else {
-        ptx::setmaxnreg_dec<kControlRegs>();
+    } else if (warp < kRotateWarp0) {
+        ptx::setmaxnreg_dec<control_regs(ROPE)>();
         if (warp == kMmaWarp)
             role_mma<D, BF16, ROPE>(p, smem, smem_ptr, tmem, sc);
         else if (warp == kTmaWarp)
             role_tma<D>(&tmK, &tmV, smem, smem_ptr, sc);
         else if (warp == kQWarp)
             role_qload<D, CAUSAL, ADDITIVE, BF16, ROPE, PACK>(&tmQ, &tmO, p, smem, smem_ptr, sc);
-        else if (ROPE && warp == kRopeWarp)
-            role_rope_q<D, BF16>(p, smem, smem_ptr, sc);
+        __syncwarp();
+    } else {
+        ptx::setmaxnreg_dec<kRotateRegs>();
+        role_rope_q<D, BF16>(p, smem, smem_ptr, sc);
         __syncwarp();
     }
 
