@@ -52,8 +52,12 @@ def test_linear_matches_fp64(M, N, K, bias, res):
 
 
 # (6000, 512): more rows than the grid has warps (two blocks of eight warps
-# per SM), so warps loop over several rows, with a ragged last pass.
-@pytest.mark.parametrize("M,H", [(333, 256), (64, 1000), (257, 4096), (16, 8192), (6000, 512)])
+# per SM), so warps loop over several rows, with a ragged last pass. Rows of
+# 1025-4096 values take the register-resident kernel (one block of eight warps
+# per SM, the next row loaded ahead): (3000, 4096) gives each warp two or three
+# rows; H = 1032 is 129 chunks of eight, one more than 32 lanes x 4.
+@pytest.mark.parametrize("M,H", [(333, 256), (64, 1000), (257, 4096), (16, 8192), (6000, 512), (3000, 4096),
+                                 (700, 1032)])
 def test_layernorm_matches_fp64(M, H):
     x = _rand((M, H), H, 2.0)
     g = (_rand((H,), 1, 0.1).float() + 1.0).to(torch.bfloat16)
