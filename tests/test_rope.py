@@ -82,6 +82,8 @@ CASES = [
     (1, 2, 2, 600, 600, 128, 2, 0, 0, 1, "f16"),         # additive mask: both sub-tiles' O staged, ragged tail
     (1, 8, 8, 600, 600, 64, 1, 0, 0, 1, "bf16"),
     (2, 16, 4, 8, 2048, 128, 1, 2040, 0, 4, "f16"),      # short prefill over a cache, four ranges
+    (1, 4, 2, 300, 400, 64, 2, 7, 3, 1, "bf16"),         # additive mask at D = 64, GQA, offsets
+    (1, 2, 2, 161, 161, 128, 1, 0, 0, 1, "bf16"),        # upper sub-tile rows end inside the second rotating warp's rows
 ]
 
 
